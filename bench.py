@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of MLA decode over a paged latent KV cache on GB300.
+
+Default workload (the headline): dense BF16 cache, B=64 requests, s_q=1,
+h_q=128 heads x 576 (512 latent + 64 RoPE), every request 8192 tokens,
+64-token pages in a seeded shuffled block table. One step = one pass of the
+hot path: split-KV schedule (mla_get_metadata) + decode (split kernel +
+combine) over the whole batch.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints ONE JSON line (rank 0). Under torchrun with N > 1 every rank runs an
+independent replica of the workload on its own GPU (weak scaling, no
+collective on the data path); the timed region is bracketed by a barrier and
+a device synchronisation and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOPS + KV GB/s (fraction of GB300 roofline), B=64 s_q=1 seqlen 8K"
+
+WORKLOADS = {
+    # name: (kind, params)
+    "dense_bf16_b64_sq1_l8192": dict(kind="dense", batch=64, s_q=1, lens=("fixed", 8192), causal=False),
+    "dense_bf16_b64_sq1_uniform": dict(kind="dense", batch=64, s_q=1, lens=("uniform", 4096, 12288), causal=False),
+    "dense_bf16_b64_sq2_causal_l8192": dict(kind="dense", batch=64, s_q=2, lens=("fixed", 8192), causal=True),
+    "dense_bf16_b64_sq2_causal_uniform": dict(kind="dense", batch=64, s_q=2, lens=("uniform", 4096, 12288),
+                                              causal=True),
+}
+DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_seqlens(w):
+    import synth
+    if w["lens"][0] == "fixed":
+        return [w["lens"][1]] * w["batch"]
+    return [int(x) for x in synth.uniform_seqlens(w["batch"], w["lens"][1], w["lens"][2], seed=2)]
+
+
+def work_counts(seqlens, s_q, causal, h_q=128):
+    """Algorithmic FLOPs and bytes of one step (no partials, no expansion)."""
+    pairs = 0
+    for L in seqlens:
+        for i in range(s_q):
+            pairs += max(0, L - (s_q - 1 - i if causal else 0))
+    flops = 2.0 * h_q * (576 + 512) * pairs
+    kv = sum(seqlens) * 576 * 2
+    B = len(seqlens)
+    qb = B * s_q * h_q * 576 * 2
+    ob = B * s_q * h_q * (512 * 2 + 4)
+    bt = sum((L + 63) // 64 for L in seqlens) * 4 + B * 4
+    return flops, kv + qb + ob + bt, kv
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_case(w, device):
+    import synth
+    seqlens = workload_seqlens(w)
+    case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device)
+    return case, seqlens
+
+
+def oracle_rate(case, seqlens, budget_s, max_requests=None):
+    """The float64 oracle on whole requests (all heads) until the time budget
+    is used; returns (flops/s, description, requests done)."""
+    import numpy as np
+    import oracle
+    import synth
+    s_q, causal = case.s_q, case.causal
+    bt = case.block_table.numpy()
+    t0 = time.perf_counter()
+    done_flops, done = 0.0, 0
+    nreq = len(seqlens) if max_requests is None else min(max_requests, len(seqlens))
+    for b in range(nreq):
+        rows = synth.paged_rows_index(bt[b], seqlens[b], case.page_block)
+        kv = oracle.to_f64(case.kv_rows[torch_index(rows, case.kv_rows.device)].cpu())
+        q = oracle.to_f64(case.q[b].cpu())
+        for i in range(s_q):
+            L = seqlens[b] - (s_q - 1 - i if causal else 0)
+            oracle.attend(q[i], kv[:max(L, 0)], case.softmax_scale)
+            done_flops += 2.0 * 128 * 1088 * max(L, 0)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done_flops / dt, f"{done} of {len(seqlens)} requests (all {case.h_q} heads, s_q={s_q})", done, dt
+
+
+def torch_index(rows, device):
+    import torch
+    return torch.from_numpy(rows).to(device)
+
+
+def run_ours(args, w, rank, world, device):
+    import torch
+    import mla_latent_kv_14_gb300 as mla
+
+    torch.cuda.set_device(device)
+    case, seqlens = build_case(w, device)
+    flops, algo_bytes, kv_bytes = work_counts(seqlens, w["s_q"], w["causal"])
+    q = case.q
+    kv = case.kvcache_paged()
+    bt = case.block_table.to(device)
+    sl = case.cache_seqlens.to(device)
+    s_q, causal = w["s_q"], w["causal"]
+    out = torch.empty(q.shape[0], s_q, 128, 512, dtype=q.dtype, device=device)
+    lse = torch.empty(q.shape[0], s_q, 128, dtype=torch.float32, device=device)
+    meta, ns = mla.mla_get_metadata(sl, s_q, 128, causal=causal)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        m, n = mla.mla_get_metadata(sl, s_q, 128, causal=causal, num_sm_parts=meta.parts)
+        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
+                                    out=out, lse=lse)
+
+    # correctness gate before timing: device status must be clean
+    step()
+    st, bits = mla.mla_read_status(device=device)
+    if st != 0:
+        raise RuntimeError(f"device status {st} (bits {bits}) before timing")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+        torch.distributed.barrier()
+    st, bits = mla.mla_read_status(device=device)
+    if st != 0:
+        raise RuntimeError(f"device status {st} (bits {bits}) after timing")
+
+    # per-kernel durations (same stream), for the roofline of the dominant kernel
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.roofline_steps)]
+    for k in range(args.roofline_steps):
+        ev[k][0].record(stream)
+        m, n = mla.mla_get_metadata(sl, s_q, 128, causal=causal, num_sm_parts=meta.parts)
+        ev[k][1].record(stream)
+        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
+                               out=out, lse=lse)
+        ev[k][2].record(stream)
+        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
+                               out=out, lse=lse)
+        ev[k][3].record(stream)
+    torch.cuda.synchronize(device)
+    t_meta = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_dec = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    t_comb = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh = q.cpu().pin_memory()
+        bth = case.block_table.pin_memory()
+        slh = case.cache_seqlens.pin_memory()
+        outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, btd, sld = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            btd.copy_(bth, non_blocking=True)
+            sld.copy_(slh, non_blocking=True)
+            m, n = mla.mla_get_metadata(sld, s_q, 128, causal=causal, num_sm_parts=meta.parts)
+            mla.mla_decode_with_kvcache(qd, kv, btd, sld, 512, m, n, softmax_scale=case.softmax_scale,
+                                        causal=causal, out=out, lse=lse)
+            outh.copy_(out, non_blocking=True)
+            lseh.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        n_e2e = max(10, args.steps // 4)
+        t0 = time.perf_counter()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        t_e2e = max(a0.elapsed_time(a1) / 1e3, 0.0) / n_e2e
+        wall = (time.perf_counter() - t0) / n_e2e
+        t_e2e = max(t_e2e, wall)
+        if world > 1:
+            t = torch.tensor([t_e2e], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        h2d = qh.numel() * qh.element_size() + bth.numel() * 4 + slh.numel() * 4
+        d2h = outh.numel() * outh.element_size() + lseh.numel() * 4
+        e2e = {"value": round(world * flops / t_e2e / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(t_e2e * 1e3, 4)}
+    return dict(elapsed=elapsed, flops=flops, algo_bytes=algo_bytes, kv_bytes=kv_bytes, t_meta=t_meta, t_dec=t_dec,
+                t_comb=t_comb, clocks=clk.summary(), e2e=e2e, parts=meta.parts, case=case, seqlens=seqlens)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--roofline-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    hbm_peak, tc_peak, tc_sus, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.cuda.set_device(device)
+        torch.distributed.init_process_group("nccl", device_id=device)
+    r = run_ours(args, w, rank, world, device)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    t_step = r["elapsed"] / args.steps
+    tflops = world * r["flops"] / t_step / 1e12
+    kv_gbs = world * r["kv_bytes"] / t_step / 1e9
+    t_roof = max(r["algo_bytes"] / (hbm_peak * 1e9), r["flops"] / (tc_peak * 1e12))
+    bound = "hbm" if r["algo_bytes"] / (hbm_peak * 1e9) >= r["flops"] / (tc_peak * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved = r["algo_bytes"] / r["t_dec"] / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "kernel": "mla_decode_dense_kernel", "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        achieved = r["flops"] / r["t_dec"] / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tc_peak, 4), "traffic": None,
+                "kernel": "mla_decode_dense_kernel", "peak_source": f"{peak_src} bf16_tflops"}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu_case = r["case"]
+        rate, desc, _, _ = oracle_rate(cpu_case, r["seqlens"], args.cpu_budget)
+        cpu = {"value": round(rate / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"float64 oracle on {desc} of this workload"}
+    line = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": 128, "d_qk": 576,
+                   "d_v": 512, "page_block": 64, "causal": w["causal"],
+                   "seqlens": (f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
+                               else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),
+                   "parallelism": f"replicas x{world}", "num_sm_parts": r["parts"],
+                   "l2": "inputs larger than L2 (KV cache %.0f MB per replica)" % (r["kv_bytes"] / 1e6)},
+        "kv_gbs": round(kv_gbs, 1), "algo_gbs": round(world * r["algo_bytes"] / t_step / 1e9, 1),
+        "roofline_time_frac": round(t_roof / t_step, 4),
+        "kernel_us": {"metadata": round(r["t_meta"] * 1e6, 2), "decode": round(r["t_dec"] * 1e6, 2),
+                      "combine": round(r["t_comb"] * 1e6, 2)},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"], "clocks": r["clocks"],
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, w, rank, world):
+    """The oracle (float64, host cores) on bounded samples of the workload."""
+    if world > 1 and rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    seqlens = workload_seqlens(w)
+    case = synth.make_dense_case(seqlens[:1] * 1, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0)
+    L = seqlens[0]
+    q = oracle.to_f64(case.q[0])
+    rows = synth.paged_rows_index(case.block_table.numpy()[0], L, 64)
+    kv = oracle.to_f64(case.kv_rows)[rows]
+    # calibrate heads per step so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle.attend(q[0], kv, case.softmax_scale)
+    t_full = time.perf_counter() - t0
+    budget = 120.0 / (args.steps + args.warmup)
+    heads = int(max(1, min(128, 128 * budget / max(t_full, 1e-6))))
+    for _ in range(args.warmup):
+        oracle.attend(q[0, :heads], kv, case.softmax_scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attend(q[0, :heads], kv, case.softmax_scale)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 2.0 * heads * 1088 * L
+    val = flops / dt / 1e12
+    sample = f"float64 oracle, one request of {L} tokens x {heads} heads per step (s_q position 0)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": 128},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

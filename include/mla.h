@@ -1,0 +1,186 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) decode over a
+ * paged, compressed latent KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed. After weight absorption every query head scores one shared
+ * 576-wide cache row per token (512 latent dims c^KV + 64 decoupled-RoPE dims
+ * k^R): score = q~ . c + q^R . k^R, and the value is the 512-wide latent c
+ * itself; decode is therefore MQA with h_kv = 1, d_k = 576, d_v = 512
+ * ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §六 '吸收' and '结果：decode
+ * 变成 MQA'). For every request b, query position i and head h:
+ *     out[b,i,h,:] = sum_t softmax_t(scale * q[b,i,h,:] . K_t) * K_t[0:512]
+ *     lse[b,i,h]   = ln sum_t exp(scale * q[b,i,h,:] . K_t)
+ * over the visible tokens t (§五 '注意力：两个 GEMM 加一个 softmax' of the same
+ * page; the kernels use the online softmax and the split-KV combine of §五/§七,
+ * which reorder but do not approximate it).
+ *
+ * Conventions for every call below:
+ *  - Pointers marked (device) are CUDA device pointers owned by the caller; the
+ *    library never allocates, frees or retains them past the call (except that
+ *    the kernels it enqueues read/write them until they complete on `stream`).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All work is enqueued asynchronously; no call synchronises the host except
+ *    mla_read_status().
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    return MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED; nothing is written then.
+ *  - Problems only visible on the device (an out-of-range page or index, a
+ *    stale metadata buffer, a pipeline wait that timed out) never trap: the
+ *    kernel sets a bit in the status word kept in the workspace, and
+ *    mla_read_status() reports it.
+ *  - All entry points are thread-safe; calls on one stream execute in order.
+ */
+#ifndef MLA_GB300_H_
+#define MLA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,      /* bad shape, pointer, alignment or flag combination */
+  MLA_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement */
+  MLA_ERR_STALE_METADATA = 3,   /* metadata computed for a different shape/lengths */
+  MLA_ERR_INDEX = 4,            /* an out-of-range page or sparse index was skipped */
+  MLA_ERR_TIMEOUT = 5,          /* a device pipeline wait gave up (kernel returned early) */
+  MLA_ERR_CUDA = 6              /* a CUDA runtime/driver call failed */
+} mla_status;
+
+typedef enum { MLA_DTYPE_BF16 = 0, MLA_DTYPE_FP16 = 1 } mla_dtype;
+
+#define MLA_HEAD_DIM_K 576
+#define MLA_HEAD_DIM_V 512
+#define MLA_FP8_ROW_BYTES 656
+
+/* Human-readable name of a status code (static string). */
+MLA_API const char* mla_status_string(int status);
+
+/* Number of work partitions ("SM parts") the decode kernels use on `device`:
+ * the number of co-resident 2-CTA clusters of the dense/FP8 decode kernel.
+ * Returns a value <= 0 on failure (no device). */
+MLA_API int mla_num_sm_parts(int device);
+
+/* Bytes of the metadata buffer for a decode shape. */
+MLA_API size_t mla_metadata_size(int batch, int s_q, int num_sm_parts);
+
+/*
+ * Split-KV work schedule ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA",
+ * §七 'split-KV：把长序列切开': the schedule decides which SM part handles which
+ * requests and KV blocks and how many pieces each request is cut into; it is
+ * computed once and reused by every layer and step of the same shape).
+ *
+ * The (request, query position) pairs v = i*batch + b ("virtual requests")
+ * are cut into 64-token tiles (visible length per query position: dense
+ * L_b, or L_b - s_q + 1 + i when causal; sparse: topk) and the tile list is
+ * cut into `num_sm_parts` contiguous ranges of nearly equal cost.
+ *
+ * cache_seqlens (device) int32 [batch]; may be NULL when topk > 0 (sparse).
+ * metadata      (device) mla_metadata_size() bytes, written.
+ * num_splits    (device) int32 [batch*s_q + 1], written: exclusive prefix sum
+ *               of the number of pieces of each virtual request.
+ * h_q must be 128 (16 for the few-heads kernel), h_kv must be 1, page_block 64.
+ * Computed entirely on the device (no host synchronisation). The decode call
+ * checks on the device that the metadata matches its own arguments and the
+ * current cache_seqlens, and reports MLA_ERR_STALE_METADATA otherwise.
+ */
+MLA_API mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                            int topk, int is_fp8, int causal, int page_block, int num_sm_parts,
+                            void* metadata, int32_t* num_splits, void* stream);
+
+/* Bytes of decode workspace (status word + fp32 split partials). */
+MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts);
+
+/*
+ * Decode attention over the latent cache ("FlashMLA 实战：MLA 注意力加速指南",
+ * §最小调用: out, lse = flash_mla_with_kvcache(q, kvcache, block_table,
+ * cache_seqlens, head_dim_v=512, metadata, num_splits, softmax_scale, causal,
+ * is_fp8_kvcache, indices)).
+ *
+ * q            (device) [batch, s_q, h_q, 576], `q_dtype`, contiguous, 16-B aligned.
+ * kvcache      (device) [num_blocks, page_block, 1, 576] of q_dtype (is_fp8 = 0), or
+ *              [num_blocks, page_block, 1, 656] uint8 rows (is_fp8 = 1, see
+ *              mla_quantize_kv_fp8), contiguous, 16-B aligned.
+ * block_table  (device) int32 [batch, max_blocks], logical page -> physical page;
+ *              may be NULL when indices != NULL.
+ * cache_seqlens(device) int32 [batch] tokens per request (ignored when indices != NULL).
+ * head_dim_v   must be 512.
+ * metadata, num_splits: from mla_get_metadata() with the same shape/flags.
+ * softmax_scale: multiplies q.K (e.g. 576^-0.5).
+ * causal       bottom-right aligned mask for s_q > 1; must be 0 with indices.
+ * indices      (device) int32 [batch, s_q, topk] absolute cache rows
+ *              (page * page_block + slot), -1 = unused slot; NULL for dense.
+ *              Rows must lie in [0, num_blocks*page_block); others are skipped
+ *              and flagged as MLA_ERR_INDEX ("拆解" page, §八 sparse indices).
+ * out          (device) [batch, s_q, h_q, 512] of q_dtype, written.
+ * lse          (device) fp32 [batch, s_q, h_q], natural log, written.
+ * workspace    (device) mla_workspace_size() bytes, 256-B aligned; its status
+ *              word must be zeroed once before first use (mla_read_status clears it).
+ * A request with no visible token gets out = 0 and lse = -inf.
+ */
+MLA_API mla_status mla_decode_with_kvcache(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
+                                   int page_block, const int32_t* block_table, int max_blocks,
+                                   const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                                   int head_dim_v, const void* metadata, const int32_t* num_splits,
+                                   int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                   const int32_t* indices, int topk, void* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two launches mla_decode_with_kvcache() is made of, for callers that
+ * schedule them separately (same arguments, same checks):
+ *  - mla_decode_splitkv: the split-KV kernel ("矩阵、注意力与 GPU：拆解 DeepGEMM 与
+ *    FlashMLA", §七 'split-KV'); requests that are one piece get their final
+ *    out/lse, the pieces of cut requests get fp32 partials (o, lse) in the
+ *    workspace;
+ *  - mla_combine_splits: merges those partials into out/lse (m = max lse_i,
+ *    o = sum o_i e^{lse_i - m} / sum e^{lse_i - m}, same section) and writes
+ *    out = 0, lse = -inf for requests with no visible token. It must follow
+ *    mla_decode_splitkv of the same arguments on the same stream.
+ */
+MLA_API mla_status mla_decode_splitkv(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
+                                      int page_block, const int32_t* block_table, int max_blocks,
+                                      const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                                      int head_dim_v, const void* metadata, const int32_t* num_splits,
+                                      int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                      const int32_t* indices, int topk, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+MLA_API mla_status mla_combine_splits(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
+                                      int page_block, const int32_t* block_table, int max_blocks,
+                                      const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                                      int head_dim_v, const void* metadata, const int32_t* num_splits,
+                                      int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                      const int32_t* indices, int topk, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Write the 656-byte FP8 cache rows ("FlashMLA 实战：MLA 注意力加速指南",
+ * §FP8 缓存怎么把 KV 压掉四成): bytes [0,512) e4m3 codes of the 512 latent dims,
+ * quantised per 128 values with scale = fp32(amax/448) (1.0 for an all-zero
+ * block) and code = round-to-nearest-even(fp32(x/scale)) saturated to +-448;
+ * bytes [512,528) the 4 scales as fp32; bytes [528,656) the 64 RoPE dims copied
+ * as bf16.
+ * kv (device) bf16 [n, 576] (row stride 576 elements); out (device) uint8 [n, 656].
+ */
+MLA_API mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the status word of `workspace`, and
+ * return the first error it records (MLA_OK if none). *bits (optional)
+ * receives the raw bits: 1 = index/page skipped, 2 = wait timeout,
+ * 4 = stale metadata.
+ */
+MLA_API mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_GB300_H_ */

@@ -1,0 +1,309 @@
+// mla_api.cu -- the C ABI declared in include/mla.h: argument checks, tensor
+// maps, launches. Every argument check happens before anything is enqueued.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "decode_dense.cuh"
+#include "params.h"
+#include "quant.cuh"
+#include "sched.cuh"
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+mla_status cuda_fail(cudaError_t e) {
+  (void)cudaGetLastError();
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+#define MLA_CUDA(x)                              \
+  do {                                           \
+    cudaError_t e_ = (x);                        \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of `elem` bytes, box [box_rows, box_cols]
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, uint64_t rows, uint64_t cols,
+              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  (void)elem;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// per-device number of co-resident 2-CTA clusters of the decode kernel
+std::atomic<int> g_parts[kMaxDevices];
+std::once_flag g_attr_once[kMaxDevices];
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t prepare_device(int dev) {
+  cudaError_t err = cudaSuccess;
+  std::call_once(g_attr_once[dev], [&] {
+    err = set_smem(dense::mla_decode_dense_kernel<false>, dense::kSmemBytes);
+    if (err == cudaSuccess) err = set_smem(dense::mla_decode_dense_kernel<true>, dense::kSmemBytes);
+    if (err == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(dense::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = dense::kSmemBytes;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      err = cudaOccupancyMaxActiveClusters(&n, dense::mla_decode_dense_kernel<false>, &cfg);
+      if (err == cudaSuccess) g_parts[dev].store(n > 0 ? n : 1);
+    }
+  });
+  return err;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported";
+    case MLA_ERR_STALE_METADATA: return "metadata does not match this call (recompute it)";
+    case MLA_ERR_INDEX: return "out-of-range page or index skipped";
+    case MLA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MLA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int mla_num_sm_parts(int device) {
+  if (device < 0 || device >= kMaxDevices) return -1;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) { (void)cudaGetLastError(); return -1; }
+  if (cur != device && cudaSetDevice(device) != cudaSuccess) { (void)cudaGetLastError(); return -1; }
+  cudaError_t e = prepare_device(device);
+  if (cur != device) cudaSetDevice(cur);
+  if (e != cudaSuccess) { (void)cudaGetLastError(); return -1; }
+  return g_parts[device].load();
+}
+
+size_t mla_metadata_size(int batch, int s_q, int parts) {
+  if (batch <= 0 || s_q <= 0 || parts <= 0) return 0;
+  return (size_t)meta_words(batch * s_q, parts) * sizeof(int32_t);
+}
+
+size_t mla_workspace_size(int batch, int s_q, int h_q, int parts) {
+  if (batch <= 0 || s_q <= 0 || h_q <= 0 || parts <= 0) return 0;
+  const int64_t S = max_splits(batch * s_q, parts);
+  return kWsHeader + (size_t)S * h_q * kDV * sizeof(float) + (size_t)S * h_q * sizeof(float);
+}
+
+mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int h_kv, int topk,
+                            int is_fp8, int causal, int page_block, int parts, void* metadata, int32_t* num_splits,
+                            void* stream) {
+  if (batch <= 0 || s_q <= 0 || parts <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
+  if (h_kv != 1 || page_block != kTile) return MLA_ERR_INVALID_ARG;
+  if (h_q != 128) return MLA_ERR_UNSUPPORTED;
+  if (!metadata || !num_splits) return MLA_ERR_INVALID_ARG;
+  if (topk == 0 && !cache_seqlens) return MLA_ERR_INVALID_ARG;
+  if (topk > 0 && causal) return MLA_ERR_INVALID_ARG;
+  if ((int64_t)batch * s_q > kMaxVreq) return MLA_ERR_UNSUPPORTED;
+  MetaParams mp{topk > 0 ? nullptr : cache_seqlens, batch, s_q, h_q, topk, is_fp8 ? 1 : 0, causal ? 1 : 0,
+                page_block, parts, static_cast<int32_t*>(metadata), num_splits};
+  const size_t smem = metadata_smem_bytes(batch * s_q);
+  if (smem > 48 * 1024) {
+    MLA_CUDA(cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  }
+  mla_metadata_kernel<<<1, kMetaThreads, smem, static_cast<cudaStream_t>(stream)>>>(mp);
+  MLA_CUDA(cudaGetLastError());
+  return MLA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+enum : int { STAGE_SPLIT = 1, STAGE_COMBINE = 2 };
+
+mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
+                       int page_block, const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens,
+                       int batch, int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
+                       int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  // ---- host-side argument checks (nothing is enqueued on failure) ----
+  if (!q || !kvcache || !out || !lse || !workspace || !metadata || !num_splits) return MLA_ERR_INVALID_ARG;
+  if (q_dtype != MLA_DTYPE_BF16 && q_dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
+  if (head_dim_v != kDV || page_block != kTile) return MLA_ERR_INVALID_ARG;
+  if (batch <= 0 || s_q <= 0 || parts <= 0 || num_blocks <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (indices && causal) return MLA_ERR_INVALID_ARG;        // the index list already fixes the key set
+  if ((indices != nullptr) != (topk > 0)) return MLA_ERR_INVALID_ARG;
+  if (!indices && (!block_table || max_blocks <= 0 || !cache_seqlens)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kvcache, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
+  if (num_blocks * (int64_t)page_block >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+  if (h_q != 128) return MLA_ERR_UNSUPPORTED;
+  if (is_fp8 || indices) return MLA_ERR_UNSUPPORTED;
+  const int64_t qrows = (int64_t)batch * s_q * h_q;
+  if (qrows >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  MLA_CUDA(cudaGetDevice(&dev));
+  if (dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  MLA_CUDA(prepare_device(dev));
+
+  const bool fp16 = q_dtype == MLA_DTYPE_FP16;
+  const CUtensorMapDataType dt = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tm_q, tm_kv;
+  if (!make_map(&tm_q, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MLA_ERR_CUDA;
+  if (!make_map(&tm_kv, kvcache, dt, 2, (uint64_t)(num_blocks * page_block), kDK, kDK * 2, 64, 64,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return MLA_ERR_CUDA;
+
+  const int64_t S = max_splits(batch * s_q, parts);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.block_table = block_table;
+  p.seqlens = cache_seqlens;
+  p.indices = indices;
+  p.kv_fp8 = nullptr;
+  p.meta = static_cast<const int32_t*>(metadata);
+  p.split_off = num_splits;
+  p.out = out;
+  p.lse = lse;
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.o_part = reinterpret_cast<float*>(ws + kWsHeader);
+  p.lse_part = p.o_part + S * h_q * kDV;
+  p.num_blocks = num_blocks;
+  p.num_rows = num_blocks * page_block;
+  p.max_blocks = max_blocks;
+  p.batch = batch;
+  p.s_q = s_q;
+  p.h_q = h_q;
+  p.topk = topk;
+  p.causal = causal ? 1 : 0;
+  p.is_fp8 = is_fp8 ? 1 : 0;
+  p.parts = parts;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stages & STAGE_SPLIT) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * parts, 1, 1);
+    cfg.blockDim = dim3(dense::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = dense::kSmemBytes;
+    cfg.stream = st;
+    if (fp16)
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<true>, tm_q, tm_kv, p));
+    else
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<false>, tm_q, tm_kv, p));
+  }
+  if (!(stages & STAGE_COMBINE)) return MLA_OK;
+
+  // combine, overlapped with the decode grid's tail (programmatic dependent launch)
+  CombineParams c{num_splits, p.o_part, p.lse_part, out, lse, batch, s_q, h_q, fp16 ? 1 : 0};
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, 1);
+  cc.blockDim = dim3(256, 1, 1);
+  cc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cc.attrs = at;
+  cc.numAttrs = 1;
+  if (fp16)
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__half>, c));
+  else
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__nv_bfloat16>, c));
+  return MLA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+#define MLA_DECODE_ARGS                                                                                        \
+  q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks, cache_seqlens, batch, s_q, h_q,         \
+      head_dim_v, metadata, num_splits, parts, softmax_scale, causal, is_fp8, indices, topk, out, lse, workspace, \
+      workspace_bytes, stream
+#define MLA_DECODE_PARAMS                                                                                         \
+  const void *q, int q_dtype, const void *kvcache, int64_t num_blocks, int page_block, const int32_t *block_table, \
+      int max_blocks, const int32_t *cache_seqlens, int batch, int s_q, int h_q, int head_dim_v,                   \
+      const void *metadata, const int32_t *num_splits, int parts, float softmax_scale, int causal, int is_fp8,     \
+      const int32_t *indices, int topk, void *out, float *lse, void *workspace, size_t workspace_bytes,            \
+      void *stream
+
+mla_status mla_decode_with_kvcache(MLA_DECODE_PARAMS) {
+  return decode_impl(STAGE_SPLIT | STAGE_COMBINE, MLA_DECODE_ARGS);
+}
+mla_status mla_decode_splitkv(MLA_DECODE_PARAMS) { return decode_impl(STAGE_SPLIT, MLA_DECODE_ARGS); }
+mla_status mla_combine_splits(MLA_DECODE_PARAMS) { return decode_impl(STAGE_COMBINE, MLA_DECODE_ARGS); }
+
+mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!kv || !out))) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  int dev = 0, sms = 0;
+  MLA_CUDA(cudaGetDevice(&dev));
+  MLA_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t want = (n + 7) / 8;
+  const int grid = (int)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
+  mla_quant_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(kv), out, n);
+  MLA_CUDA(cudaGetLastError());
+  return MLA_OK;
+}
+
+mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  MLA_CUDA(cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st));
+  MLA_CUDA(cudaStreamSynchronize(st));
+  MLA_CUDA(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st));
+  MLA_CUDA(cudaStreamSynchronize(st));
+  if (bits) *bits = v;
+  if (v & STATUS_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (v & STATUS_STALE) return MLA_ERR_STALE_METADATA;
+  if (v & STATUS_INDEX) return MLA_ERR_INDEX;
+  return MLA_OK;
+}
+
+}  // extern "C"

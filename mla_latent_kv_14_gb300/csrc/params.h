@@ -1,0 +1,79 @@
+// params.h -- kernel parameter blocks and the metadata layout shared by the
+// host entry points and the kernels.
+#pragma once
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kTile = 64;         // tokens per KV tile (= page_block)
+constexpr int kDK = 576;          // latent 512 + RoPE 64
+constexpr int kDV = 512;
+constexpr int kRowBytesFp8 = 656;
+constexpr int kPieceOverhead = 2; // schedule cost of starting a piece, in tiles
+
+// ---- metadata (int32 words) ----
+// header
+enum : int {
+  H_MAGIC = 0, H_BATCH, H_SQ, H_HQ, H_TOPK, H_FP8, H_CAUSAL, H_PAGE, H_PARTS, H_HASH,
+  H_NPIECES, H_VREQ, H_WORDS = 16
+};
+constexpr int32_t kMetaMagic = 0x31414C4D;  // "MLA1"
+// one record per SM part: first piece (v, tile), end (v, tile exclusive),
+// split ordinal of the first piece
+enum : int { P_BV = 0, P_BT, P_EV, P_ET, P_SPLIT, P_WORDS = 8 };
+
+__host__ __device__ inline int meta_words(int vreq, int parts) {
+  (void)vreq;
+  return H_WORDS + parts * P_WORDS;
+}
+
+// hash of the per-request lengths (or topk) baked into the metadata so the
+// decode kernel can tell that it is being reused for a different problem
+__host__ __device__ inline uint32_t hash_step(uint32_t h, uint32_t x) {
+  h ^= x + 0x9E3779B9u + (h << 6) + (h >> 2);
+  return h;
+}
+
+// ---- workspace ----
+// [0, 256): status word; then o_part fp32 [max_splits, h_q, 512]; then
+// lse_part fp32 [max_splits, h_q]
+constexpr size_t kWsHeader = 256;
+__host__ __device__ inline int64_t max_splits(int vreq, int parts) { return (int64_t)vreq + parts; }
+
+struct MetaParams {
+  const int32_t* seqlens;   // [batch] or null (sparse)
+  int batch, s_q, h_q, topk, is_fp8, causal, page_block, parts;
+  int32_t* meta;
+  int32_t* split_off;       // [vreq + 1]
+};
+
+struct DecodeParams {
+  const int32_t* block_table;  // [batch, max_blocks] (dense)
+  const int32_t* seqlens;      // [batch]
+  const int32_t* indices;      // [batch, s_q, topk] (sparse) or null
+  const uint8_t* kv_fp8;       // raw fp8 rows (fp8 kernels)
+  const int32_t* meta;
+  const int32_t* split_off;
+  void* out;                   // [batch, s_q, h_q, 512], q dtype
+  float* lse;                  // [batch, s_q, h_q]
+  float* o_part;               // [max_splits, h_q, 512]
+  float* lse_part;             // [max_splits, h_q]
+  uint32_t* status;
+  int64_t num_blocks;
+  int64_t num_rows;            // num_blocks * page_block
+  int max_blocks;
+  int batch, s_q, h_q, topk, causal, is_fp8, parts;
+  float scale_log2;            // softmax_scale * log2(e)
+};
+
+struct CombineParams {
+  const int32_t* split_off;
+  const float* o_part;
+  const float* lse_part;
+  void* out;
+  float* lse;
+  int batch, s_q, h_q;
+  int fp16;
+};
+
+}  // namespace mla

@@ -1,0 +1,282 @@
+// sched.cuh -- split-KV work schedule and the split combine.
+//
+// Schedule ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §七 'split-KV'):
+// the (request, query-position) pairs are cut into 64-token tiles; the tile
+// list, with a fixed cost per piece, is cut into `parts` contiguous ranges of
+// nearly equal cost, one per persistent 2-CTA cluster. A request cut by a
+// range boundary becomes several pieces whose partial (o, lse) the combine
+// merges: m = max lse_i, o = sum o_i e^{lse_i - m} / sum e^{lse_i - m}
+// (same section, the merge formula of online softmax).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+// visible tokens and tiles of virtual request v = i*batch + b
+__device__ __forceinline__ int vreq_tiles(const int32_t* seqlens, int topk, int batch, int s_q, int causal,
+                                          int v, int* len_out) {
+  int L;
+  if (topk > 0) {
+    L = topk;
+  } else {
+    const int b = v % batch, i = v / batch;
+    L = seqlens[b];
+    if (causal) L = L - s_q + 1 + i;
+  }
+  L = L < 0 ? 0 : L;
+  *len_out = L;
+  return (L + kTile - 1) / kTile;
+}
+
+// Fingerprint of the per-request lengths (or of topk) baked into the
+// metadata; a sum of mixed (index, length) words, so one warp computes it in
+// parallel. Every lane of the calling warp must call it; all get the result.
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7FEB352Du;
+  x ^= x >> 15;
+  x *= 0x846CA68Bu;
+  x ^= x >> 16;
+  return x;
+}
+__device__ __forceinline__ uint32_t lengths_hash_warp(const int32_t* seqlens, int batch, int topk) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h = 0;
+  if (topk > 0) {
+    h = lane == 0 ? mix32((uint32_t)topk ^ 0xA5A5A5A5u) : 0u;
+  } else {
+    for (int b = lane; b < batch; b += 32) h += mix32((uint32_t)seqlens[b] * 0x9E3779B1u + mix32((uint32_t)b));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+  return h ^ (uint32_t)batch;
+}
+
+constexpr int kMetaThreads = 1024;
+constexpr int kMaxVreq = 8192;   // virtual requests the schedule kernel holds in shared memory
+
+// block-wide exclusive scan of one int64 per thread; returns the block total
+__device__ __forceinline__ long long block_exclusive_scan(long long x, long long* warp_tot, long long& excl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+    long long wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;          // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = wi; // block total
+  }
+  __syncthreads();
+  excl = inc - x + warp_tot[warp];
+  const long long tot = warp_tot[32];
+  __syncthreads();
+  return tot;
+}
+
+// The schedule as a closed form, computed by one block:
+//  * request v costs n_v + kPieceOverhead (0 if it has no tile); C_v is the
+//    exclusive prefix sum of the costs and `total` their sum;
+//  * part p owns the cost interval [p*per, (p+1)*per), per = ceil(total/parts)
+//    (at least kPieceOverhead + 1); position x maps to the tile cursor
+//    (v, max(0, x - C_v - kPieceOverhead)) of the request whose cost interval
+//    holds x, so a part runs from cursor(p*per) to cursor((p+1)*per);
+//  * a request is cut once per part boundary that falls on one of its tiles
+//    other than its first.
+__global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p) {
+  extern __shared__ long long sh[];
+  const int V = p.batch * p.s_q;
+  long long* C = sh;                                        // [V + 1]
+  int* n = reinterpret_cast<int*>(C + V + 1);               // [V]
+  int* nsplit = n + V;                                      // [V]
+  int* firstp = nsplit + V;                                 // [V]
+  __shared__ long long warp_tot[33];
+  __shared__ long long carry;
+  if (threadIdx.x == 0) carry = 0;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    int L;
+    n[v] = vreq_tiles(p.seqlens, p.topk, p.batch, p.s_q, p.causal, v, &L);
+    nsplit[v] = 0;
+    firstp[v] = 0x7fffffff;
+  }
+  __syncthreads();
+  for (int base = 0; base < V; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    const long long c = v < V && n[v] ? (long long)n[v] + kPieceOverhead : 0;
+    long long excl;
+    const long long tot = block_exclusive_scan(c, warp_tot, excl);
+    if (v < V) C[v] = carry + excl;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  const long long total = carry;
+  if (threadIdx.x == 0) C[V] = total;
+  __syncthreads();
+  long long per = total > 0 ? (total + p.parts - 1) / p.parts : 1;
+  if (per < kPieceOverhead + 1) per = kPieceOverhead + 1;
+  auto cursor = [&](long long x, int& cv, int& ct) {
+    if (x >= total) { cv = V; ct = 0; return; }
+    int lo = 0, hi = V - 1;                 // largest v with C[v] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (C[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    cv = lo;
+    const long long t = x - C[lo] - kPieceOverhead;
+    ct = t > 0 ? (int)t : 0;
+  };
+  // part boundaries that cut a request
+  for (int q = 1 + threadIdx.x; q < p.parts; q += blockDim.x) {
+    int cv, ct;
+    const long long x = (long long)q * per;
+    cursor(x < total ? x : total, cv, ct);
+    if (cv < V && ct > 0) {
+      atomicAdd(&nsplit[cv], 1);
+      atomicMin(&firstp[cv], q);
+    }
+  }
+  __syncthreads();
+  // pieces per request -> exclusive prefix (num_splits)
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < V; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    const long long c = v < V ? (long long)((n[v] ? 1 : 0) + nsplit[v]) : 0;
+    long long excl;
+    const long long tot = block_exclusive_scan(c, warp_tot, excl);
+    if (v < V) p.split_off[v] = (int32_t)(carry + excl);
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.split_off[V] = (int32_t)carry;
+  // part records
+  int32_t* rec0 = p.meta + H_WORDS;
+  for (int q = threadIdx.x; q < p.parts; q += blockDim.x) {
+    int bv, bt, ve, te;
+    const long long x0 = (long long)q * per, x1 = (long long)(q + 1) * per;
+    cursor(x0 < total ? x0 : total, bv, bt);
+    cursor(x1 < total ? x1 : total, ve, te);
+    int32_t* r = rec0 + q * P_WORDS;
+    if (bv >= V || (bv == ve && bt == te)) {
+      r[P_BV] = -1;
+      r[P_BT] = r[P_EV] = r[P_ET] = r[P_SPLIT] = 0;
+    } else {
+      r[P_BV] = bv;
+      r[P_BT] = bt;
+      r[P_EV] = te > 0 ? ve : ve - 1;
+      r[P_ET] = te > 0 ? te : 0x7fffffff;
+      r[P_SPLIT] = bt > 0 ? q - firstp[bv] + 1 : 0;
+    }
+  }
+  const uint32_t fp = threadIdx.x < 32 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
+  if (threadIdx.x == 0) {
+    int32_t* h = p.meta;
+    h[H_MAGIC] = kMetaMagic;
+    h[H_BATCH] = p.batch;
+    h[H_SQ] = p.s_q;
+    h[H_HQ] = p.h_q;
+    h[H_TOPK] = p.topk;
+    h[H_FP8] = p.is_fp8;
+    h[H_CAUSAL] = p.causal;
+    h[H_PAGE] = p.page_block;
+    h[H_PARTS] = p.parts;
+    h[H_HASH] = (int32_t)fp;
+    h[H_NPIECES] = (int32_t)carry;
+    h[H_VREQ] = V;
+  }
+}
+
+__host__ __device__ inline size_t metadata_smem_bytes(int vreq) {
+  return (size_t)(vreq + 1) * sizeof(long long) + (size_t)vreq * 3 * sizeof(int);
+}
+
+// True when the metadata was built for exactly this call; `fp` is the
+// lengths fingerprint of this call (lengths_hash_warp).
+__device__ __forceinline__ bool metadata_matches(const DecodeParams& p, int page_block, uint32_t fp) {
+  const int32_t* h = p.meta;
+  return h[H_MAGIC] == kMetaMagic && h[H_BATCH] == p.batch && h[H_SQ] == p.s_q && h[H_HQ] == p.h_q &&
+         h[H_TOPK] == p.topk && h[H_FP8] == p.is_fp8 && h[H_CAUSAL] == p.causal && h[H_PAGE] == page_block &&
+         h[H_PARTS] == p.parts && h[H_VREQ] == p.batch * p.s_q && (uint32_t)h[H_HASH] == fp;
+}
+
+// Merge the split partials of each virtual request. grid = (vreq, h_q/16),
+// block = 256: each warp merges two heads, each lane 16 of the 512 dims.
+// Requests with a single piece were finished by the decode kernel; requests
+// with no visible token get out = 0, lse = -inf here.
+template <typename OutT>
+__global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
+  pdl_wait();  // the decode grid has completed and its writes are visible
+  const int v = blockIdx.x;
+  const int b = v % p.batch, i = v / p.batch;
+  const int off = p.split_off[v];
+  const int ns = p.split_off[v + 1] - off;
+  if (ns == 1) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = blockIdx.y * 16 + warp * 2 + hh;
+    if (h >= p.h_q) break;
+    const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
+    OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, p.lse_part[(int64_t)(off + s) * p.h_q + h]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int s = 0; s < ns; ++s) {
+        const float ls = p.lse_part[(int64_t)(off + s) * p.h_q + h];
+        const float w = expf(ls - mx);
+        wsum += w;
+        const float4* src = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s) * p.h_q + h) * kDV);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = src[j * 32 + lane];
+          acc[4 * j + 0] += w * x.x;
+          acc[4 * j + 1] += w * x.y;
+          acc[4 * j + 2] += w * x.z;
+          acc[4 * j + 3] += w * x.w;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int d = j * 128 + lane * 4;
+      if constexpr (sizeof(OutT) == 2) {
+        uint32_t lo, hi;
+        if constexpr (std::is_same<OutT, __half>::value) {
+          lo = pack_f16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
+          hi = pack_f16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+        } else {
+          lo = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
+          hi = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+        }
+        *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
+      }
+    }
+    if (lane == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+  }
+}
+
+}  // namespace mla

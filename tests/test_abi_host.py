@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+entry point include/mla.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import mla_latent_kv_14_gb300 as m
+    if not os.path.exists(m.LIB_PATH):
+        from mla_latent_kv_14_gb300 import build
+        build.build()
+    return m.load_library()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for must in ["mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits", "mla_quantize_kv_fp8", "mla_read_status",
+                 "mla_metadata_size", "mla_workspace_size", "mla_num_sm_parts", "mla_status_string"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import mla_latent_kv_14_gb300 as m
+    out = subprocess.run(["nm", "-D", "--defined-only", m.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (mla_\w+)", out))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+    for n in declared_symbols():
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.mla_status_string(code)
+    assert b"unknown" in lib.mla_status_string(99)
+
+
+def test_sizes(lib):
+    assert lib.mla_metadata_size(64, 1, 76) == 4 * (16 + 8 * 76)
+    ws = lib.mla_workspace_size(64, 1, 128, 76)
+    assert ws == 256 + (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4
+    assert lib.mla_workspace_size(0, 1, 128, 76) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: checks fail first
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, q_dtype=0, kv=FAKE, num_blocks=8, page_block=64, bt=FAKE, max_blocks=8, sl=FAKE, batch=2,
+             s_q=1, h_q=128, dv=512, meta=FAKE, ns=FAKE, parts=4, scale=576 ** -0.5, causal=0, fp8=0, idx=None,
+             topk=0, out=FAKE, lse=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.mla_decode_with_kvcache(a["q"], a["q_dtype"], a["kv"], a["num_blocks"], a["page_block"], a["bt"],
+                                       a["max_blocks"], a["sl"], a["batch"], a["s_q"], a["h_q"], a["dv"], a["meta"],
+                                       a["ns"], a["parts"], a["scale"], a["causal"], a["fp8"], a["idx"], a["topk"],
+                                       a["out"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=256), 1),                                  # head_dim_v must be 512
+    (dict(page_block=32), 1),
+    (dict(q=None), 1),
+    (dict(q_dtype=7), 1),
+    (dict(idx=FAKE, topk=2048, causal=1), 1),           # causal with indices
+    (dict(idx=FAKE, topk=0), 1),                        # indices without topk
+    (dict(bt=None), 1),                                 # dense needs a block table
+    (dict(q=ctypes.c_void_p((1 << 20) + 2)), 1),        # misaligned q
+    (dict(ws=ctypes.c_void_p((1 << 20) + 16)), 1),      # workspace needs 256-B alignment
+    (dict(wsb=100), 1),                                 # workspace too small
+    (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(batch=0), 1),
+    (dict(h_q=64), 2),                                  # not implemented
+])
+def test_decode_argument_checks(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_metadata_argument_checks(lib):
+    f = lib.mla_get_metadata
+    assert f(FAKE, 2, 1, 128, 2, 0, 0, 0, 64, 4, FAKE, FAKE, None) == 1        # h_kv != 1
+    assert f(FAKE, 2, 1, 128, 1, 0, 0, 0, 32, 4, FAKE, FAKE, None) == 1        # page_block
+    assert f(None, 2, 1, 128, 1, 0, 0, 0, 64, 4, FAKE, FAKE, None) == 1        # dense needs lengths
+    assert f(None, 2, 1, 128, 1, 64, 1, 1, 64, 4, FAKE, FAKE, None) == 1       # sparse + causal
+    assert f(FAKE, 2, 1, 128, 1, 0, 0, 0, 64, 0, FAKE, FAKE, None) == 1        # parts
+
+
+def test_quantize_argument_checks(lib):
+    assert lib.mla_quantize_kv_fp8(FAKE, FAKE, -1, None) == 1
+    assert lib.mla_quantize_kv_fp8(ctypes.c_void_p((1 << 20) + 8), FAKE, 4, None) == 1
+    assert lib.mla_quantize_kv_fp8(FAKE, FAKE, 0, None) == 0
