@@ -13,9 +13,9 @@
 // How the work is laid out on GB300. The fp32 O for 128 heads x 512 fills the
 // whole 128-lane x 512-column tensor memory of one SM, so the two CTAs of the
 // cluster split the latent dimension: CTA r keeps O[:, 256r : 256r+256] in TMEM
-// (256 columns) and loads only its own 64-wide column chunks of Q and of every
-// KV tile -- CTA 0 chunks {0,1,2,3} plus the RoPE chunk 8, CTA 1 chunks
-// {4,5,6,7}. Each CTA computes a partial S over its chunks with single-CTA
+// (256 columns) and loads only its own part of Q and of every KV tile: CTA r
+// the latent dims [256r, 256r+256) and the RoPE dims [512+32r, 544+32r).
+// Each CTA computes a partial S over its dims with single-CTA
 // UMMA (M=128 heads, N=64 tokens); the two fp32 partials are exchanged through
 // distributed shared memory and summed, so both CTAs hold the full S, run the
 // same softmax (bit-identical), and accumulate P . V for their own half of the
@@ -25,10 +25,30 @@
 // kernel pairs two CTAs over DSM -- Crossover; here the pair exists because
 // TMEM is full.)
 //
+// Memory map. TMEM (512 columns): O half [0,256), S buffers [256,320) and
+// [320,384), and this CTA's 256 latent dims of Q as the UMMA A operand
+// [384,512) (column j = bf16 pair (2j, 2j+1) of head row = lane). Shared
+// memory: the peer's partial scores (fp32, 32 KB), this CTA's partial scores
+// staged for the copy to the peer (32 KB), P (bf16, 16 KB), the CTA's 32 RoPE
+// dims of Q (8 KB) and a 3-slot ring of KV tiles (36 KB each: four 64-wide
+// latent chunks, 128-byte swizzled, and one 32-wide RoPE chunk, 64-byte
+// swizzled, of 64 tokens). The producer also prefetches the tiles beyond the
+// ring into L2.
+//
 // Warp roles (256 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM
 // and lane 0 issues UMMA; warps 4-7 are the softmax / exchange / epilogue
-// warps, thread h <-> TMEM lane h <-> head h. Warps 2-3 only take part in
-// set-up and tear-down.
+// warps, thread h <-> TMEM lane h <-> head h; they also copy each piece's Q
+// rows into TMEM. Warps 2-3 only take part in set-up and tear-down.
+//
+// Pipeline. The exchange of a tile's partial scores is one bulk shared-to-
+// shared copy into the peer (the bytes complete on the peer's mbarrier); the
+// buffer-free signal is one remote arrive per warp. The softmax loop runs
+// "receive tile g, send tile g+1, softmax of tile g", so each exchange is in
+// flight while the other tile's math runs. The UMMA issuer polls its inputs
+// and issues whichever of QK^T / P.V is ready, so neither waits behind the
+// other. Measured on GB300: DSM moves about 18 B/clk per SM,
+// and small single-CTA UMMAs cost 50-70 cycles each to issue, so these two,
+// not the shared-memory ring, bound the tile rate.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,31 +60,38 @@
 namespace mla {
 namespace dense {
 
-constexpr int kNS = 2;                     // KV ring slots (tiles)
-constexpr int kMaxChunks = 5;              // 64-wide column chunks per CTA
-constexpr int kQChunk = 128 * 128;         // 128 rows x 64 x 2 B
+constexpr int kNS = 3;                     // KV ring slots (tiles)
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
-constexpr int kSlot = kMaxChunks * kKChunk;
+constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
+constexpr int kSlot = 4 * kKChunk + kRChunk;
+constexpr int kPrefetch = kNS;             // tiles ahead of the ring prefetched into L2
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
+constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
+constexpr uint32_t kXBytes = 128 * 256;    // one partial-score message
 
 // shared memory map (offsets from a 1024-B aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_RING = OFF_Q + kMaxChunks * kQChunk;
-constexpr uint32_t OFF_P = OFF_RING + kNS * kSlot;
-constexpr uint32_t OFF_SX = OFF_P + 128 * 128;          // 128 rows x 64 fp32
-constexpr uint32_t OFF_BAR = OFF_SX + 128 * 256;
+constexpr uint32_t OFF_XR = 0;                          // peer's partial: 128 rows x 64 fp32
+constexpr uint32_t OFF_XS = OFF_XR + kXBytes;           // own partial, staged for the copy
+constexpr uint32_t OFF_P = OFF_XS + kXBytes;            // 128 rows x 64 bf16
+constexpr uint32_t OFF_QR = OFF_P + 128 * 128;          // 32 RoPE dims of Q: 128 rows x 64 B
+constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
+constexpr uint32_t OFF_BAR = OFF_RING + kNS * kSlot;
 enum : uint32_t {
   B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY, B_SFULL, B_SEMPTY = B_SFULL + 2,
   B_PFULL = B_SEMPTY + 2, B_PEMPTY, B_OEMPTY, B_XFULL, B_XEMPTY, B_DRAIN, B_COUNT
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;    // tmem slot, abort flag, ok flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
+constexpr uint32_t kSoftmaxBar = 1;                     // named barrier of the 128 softmax threads
 
-__device__ __forceinline__ int chunk_id(uint32_t rank, int ci) { return rank == 0 ? (ci < 4 ? ci : 8) : 4 + ci; }
 
 // iteration over the pieces of one SM part (every role walks the same list)
+struct Piece {
+  int v, t0, t1, len, split;
+  bool fin;
+};
 struct PieceIter {
   const DecodeParams* p;
   int bv, bt, ev, et, first_split;
@@ -77,30 +104,43 @@ struct PieceIter {
     v = bv - 1;
   }
   // advance to the next non-empty piece; false when done
-  __device__ __forceinline__ bool next(int& vv, int& t0, int& t1, int& len, int& split, bool& fin) {
+  __device__ __forceinline__ bool next(Piece& pc) {
     while (++v <= ev) {
+      int len;
       const int n = vreq_tiles(p->seqlens, p->topk, p->batch, p->s_q, p->causal, v, &len);
-      t0 = (v == bv) ? bt : 0;
-      t1 = (v == ev) ? et : n;
+      int t0 = (v == bv) ? bt : 0;
+      int t1 = (v == ev) ? et : n;
       t0 = t0 < 0 ? 0 : t0;
       t1 = t1 > n ? n : t1;
       if (t1 <= t0) continue;
       const int ord = (v == bv) ? first_split : 0;
       const int off = p->split_off[v];
       const int ns = p->split_off[v + 1] - off;
-      split = off + ord;
-      fin = (ns == 1);
-      vv = v;
+      pc.v = v; pc.t0 = t0; pc.t1 = t1; pc.len = len; pc.split = off + ord; pc.fin = (ns == 1);
       return true;
     }
     return false;
   }
 };
 
+__device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
+
+// valid tokens of tile t of a dense request (0 if its page is out of range)
+__device__ __forceinline__ int dense_valid(const DecodeParams& p, int b, int t, int len, bool report) {
+  int nv = len - t * kTile;
+  nv = nv > kTile ? kTile : nv;
+  const int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
+  if (page < 0 || page >= p.num_blocks) {
+    if (report) atomicOr(p.status, STATUS_INDEX);
+    nv = 0;
+  }
+  return nv;
+}
+
 template <bool kFp16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_dense_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                            const DecodeParams p) {
+    mla_decode_dense_kernel(const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_kv,
+                            const __grid_constant__ CUtensorMap tm_kvr, const DecodeParams p) {
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,7 +149,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = rank ^ 1u;
   const int part = (int)cluster_id_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqc = rank == 0 ? 5 : 4;  // own column chunks
 
   auto bar = [&](uint32_t i) { return sb + OFF_BAR + 8u * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -124,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QFULL), 128 + 1);  // softmax threads (latent into TMEM) + RoPE TMA
     mbar_init(bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
@@ -133,8 +172,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_PFULL), 128);
     mbar_init(bar(B_PEMPTY), 1);
     mbar_init(bar(B_OEMPTY), 128);
-    mbar_init(bar(B_XFULL), 128);
-    mbar_init(bar(B_XEMPTY), 128);
+    mbar_init(bar(B_XFULL), 1);    // own expect_tx + the peer's copied bytes
+    mbar_init(bar(B_XEMPTY), 4);   // one arrive per peer softmax warp
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0u;
     *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
@@ -147,119 +186,152 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote arrive
+  cluster_sync();  // the peer's barriers exist before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool ok = *ok_flag != 0u;
 
   if (ok && warp == 0 && lane == 0) {
-    // ---------------- producer: Q chunks per piece, KV chunks per tile ----------------
-    prefetch_tmap(&tm_q);
+    // ---------------- producer: RoPE dims of Q per piece, KV chunks per tile ----------------
+    prefetch_tmap(&tm_qr);
     prefetch_tmap(&tm_kv);
+    prefetch_tmap(&tm_kvr);
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
+    const int xr = 512 + 32 * (int)rank;  // RoPE column of this CTA
     PieceIter it(p, part);
-    int v, t0, t1, len, split;
-    bool fin;
+    Piece pc;
     int g = 0, qn = 0;
-    bool issued[kNS] = {};
-    uint32_t last_par[kNS] = {};
-    bool q_issued = false;
-    uint32_t q_par = 0;
-    while (it.next(v, t0, t1, len, split, fin)) {
+    int last_g[kNS];
+    for (int s = 0; s < kNS; ++s) last_g[s] = -1;
+    int q_last = -1;
+    bool stop = false;
+    auto page_of = [&](int b, int t) {
+      int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
+      return (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the softmax warps
+    };
+    auto prefetch_tile = [&](int page) {
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) tma_prefetch_2d(&tm_kv, 256 * (int)rank + 64 * ci, page * kTile);
+      tma_prefetch_2d(&tm_kvr, xr, page * kTile);
+    };
+    while (!stop && it.next(pc)) {
+      const int b = pc.v % p.batch, i = pc.v / p.batch;
       if (!wait(bar(B_QEMPTY), (qn & 1) ^ 1, guard)) break;
-      const int b = v % p.batch, i = v / p.batch;
-      const int qrow = (b * p.s_q + i) * 128;
-      mbar_arrive_expect_tx(bar(B_QFULL), nqc * kQChunk);
-      for (int ci = 0; ci < nqc; ++ci)
-        tma_load_2d(sb + OFF_Q + ci * kQChunk, &tm_q, bar(B_QFULL), 64 * chunk_id(rank, ci), qrow, pol_q);
-      q_issued = true;
-      q_par = qn & 1;
+      mbar_arrive_expect_tx(bar(B_QFULL), 128 * 64);
+      tma_load_2d(sb + OFF_QR, &tm_qr, bar(B_QFULL), xr, (b * p.s_q + i) * 128, pol_q);
+      q_last = qn;
       ++qn;
-      bool stop = false;
-      for (int t = t0; t < t1; ++t, ++g) {
+      for (int t = pc.t0; t < pc.t0 + kNS && t < pc.t1; ++t) prefetch_tile(page_of(b, t));
+      for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const int s = g % kNS;
+        const int page = page_of(b, t);
+        if (t + kPrefetch < pc.t1) prefetch_tile(page_of(b, t + kPrefetch));
         if (!wait(bar(B_EMPTY + s), ((g / kNS) & 1) ^ 1, guard)) { stop = true; break; }
-        int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-        if (page < 0 || page >= p.num_blocks) page = 0;  // tile is masked by the softmax warps
-        mbar_arrive_expect_tx(bar(B_FULL + s), nqc * kKChunk);
-        for (int ci = 0; ci < nqc; ++ci)
-          tma_load_2d(sb + OFF_RING + s * kSlot + ci * kKChunk, &tm_kv, bar(B_FULL + s), 64 * chunk_id(rank, ci),
-                      page * kTile, pol_kv);
-        issued[s] = true;
-        last_par[s] = (g / kNS) & 1;
+        const uint32_t slot = sb + OFF_RING + s * kSlot;
+        mbar_arrive_expect_tx(bar(B_FULL + s), kSlot);
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci)
+          tma_load_2d(slot + ci * kKChunk, &tm_kv, bar(B_FULL + s), 256 * (int)rank + 64 * ci, page * kTile, pol_kv);
+        tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(B_FULL + s), xr, page * kTile, pol_kv);
+        last_g[s] = g;
       }
-      if (stop) break;
     }
     // never leave with a copy in flight into this CTA's shared memory
     for (int s = 0; s < kNS; ++s)
-      if (issued[s]) {
+      if (last_g[s] >= 0) {
         const uint64_t t_0 = globaltimer();
-        while (!mbar_try_wait(bar(B_FULL + s), last_par[s]) && globaltimer() - t_0 < 200000000ull) {}
+        while (!mbar_try_wait(bar(B_FULL + s), (last_g[s] / kNS) & 1) && globaltimer() - t_0 < 200000000ull) {}
       }
-    if (q_issued) {
+    if (q_last >= 0) {
       const uint64_t t_0 = globaltimer();
-      while (!mbar_try_wait(bar(B_QFULL), q_par) && globaltimer() - t_0 < 200000000ull) {}
+      while (!mbar_try_wait(bar(B_QFULL), q_last & 1) && globaltimer() - t_0 < 200000000ull) {}
     }
   } else if (ok && warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer ----------------
+    // ---------------- UMMA issuer: issues whichever of QK^T / P.V is ready ----------------
     constexpr uint32_t idesc_qk = idesc_f16(128, 64, !kFp16, false, false);
     constexpr uint32_t idesc_pv = idesc_f16(128, 256, !kFp16, false, true);
+    // descriptors: +2 in the low word advances the start address by 32 B (16
+    // elements of K), +128 by 2048 B (16 tokens of the MN-major V operand)
+    const uint64_t d_p = sdesc_sw128(sb + OFF_P, 16, 1024);
+    const uint64_t d_qr = sdesc_sw64(sb + OFF_QR, 16, 512);
     PieceIter it(p, part);
-    int v, t0, t1, len, split;
-    bool fin;
-    int g = 0, qn = 0, piece = 0;
-    int pend_g = -1, pend_piece = 0;
-    bool pend_first = false, failed = false;
-    auto issue_pv = [&](int gp, bool first, int pc) -> bool {
-      if (!wait(bar(B_PFULL), gp & 1, guard)) return false;
-      if (first && pc > 0 && !wait(bar(B_OEMPTY), (pc - 1) & 1, guard)) return false;
-      tc_fence_after();
-      const uint32_t slot = sb + OFF_RING + (gp % kNS) * kSlot;
+    Piece pc;
+    bool have = it.next(pc);
+    int qk_t = have ? pc.t0 : 0;   // next QK^T tile within the current piece
+    int qk_g = 0, pv_g = 0;        // next global tile for QK^T / P.V
+    int k_piece = 0;               // piece index of qk_g
+    bool q_ready = false;
+    uint32_t first_bits = 0;       // bit (g & 31): tile g is the first of its piece
+    int piece_of[4] = {0, 0, 0, 0};
+    uint64_t t_last = globaltimer();
+    bool failed = false;
+    while (true) {
+      bool progressed = false;
+      if (have) {
+        if (!q_ready && mbar_test(bar(B_QFULL), k_piece & 1)) q_ready = true;
+        const int s = qk_g % kNS, sbuf = qk_g & 1;
+        if (q_ready && mbar_test(bar(B_FULL + s), (qk_g / kNS) & 1) &&
+            mbar_test(bar(B_SEMPTY + sbuf), ((qk_g >> 1) & 1) ^ 1)) {
+          tc_fence_after();
+          const uint32_t dS = tmem + kColS + 64u * sbuf;
+          const uint32_t slot = sb + OFF_RING + s * kSlot;
+          const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
+          const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t a = sdesc_sw128(sb + OFF_P + 32 * k, 16, 1024);
-        const uint64_t bdesc = sdesc_sw128(slot + k * 2048, kKChunk, 1024);  // MN-major V: 16 tokens per step
-        umma_ss(tmem, a, bdesc, idesc_pv, (first && k == 0) ? 0u : 1u);
-      }
-      umma_commit(bar(B_PEMPTY));
-      umma_commit(bar(B_EMPTY + gp % kNS));
-      return true;
-    };
-    while (!failed && it.next(v, t0, t1, len, split, fin)) {
-      if (!wait(bar(B_QFULL), qn & 1, guard)) break;
-      ++qn;
-      for (int t = t0; t < t1; ++t, ++g) {
-        const int s = g % kNS, sbuf = g & 1;
-        if (!wait(bar(B_FULL + s), (g / kNS) & 1, guard) ||
-            !wait(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t slot = sb + OFF_RING + s * kSlot;
-        const uint32_t dS = tmem + kColS + 64u * sbuf;
-        for (int ci = 0; ci < nqc; ++ci) {
+          for (int ci = 0; ci < 4; ++ci) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc_sw128(sb + OFF_Q + ci * kQChunk + 32 * k, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(slot + ci * kKChunk + 32 * k, 16, 1024);
-            umma_ss(dS, a, bdesc, idesc_qk, (ci | k) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              umma_ts(dS, tmem + kColQ + 32u * ci + 8u * k, d_k + (uint64_t)(ci * (kKChunk >> 4) + 2 * k), idesc_qk,
+                      (ci | k) ? 1u : 0u);
           }
+          umma_ss(dS, d_qr, d_kr, idesc_qk, 1u);
+          umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qk, 1u);
+          umma_commit(bar(B_SFULL + sbuf));
+          const bool first = qk_t == pc.t0;
+          first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
+          piece_of[qk_g & 3] = k_piece;
+          ++qk_g;
+          if (++qk_t == pc.t1) {
+            umma_commit(bar(B_QEMPTY));
+            have = it.next(pc);
+            if (have) qk_t = pc.t0;
+            ++k_piece;
+            q_ready = false;
+          }
+          progressed = true;
         }
-        umma_commit(bar(B_SFULL + sbuf));
-        if (t == t1 - 1) umma_commit(bar(B_QEMPTY));
-        if (pend_g >= 0 && !issue_pv(pend_g, pend_first, pend_piece)) {
+      }
+      if (pv_g < qk_g && mbar_test(bar(B_PFULL), pv_g & 1)) {
+        const bool first = (first_bits >> (pv_g & 31)) & 1u;
+        const int pk = piece_of[pv_g & 3];
+        if (!first || pk == 0 || mbar_test(bar(B_OEMPTY), (pk - 1) & 1)) {
+          tc_fence_after();
+          const uint64_t d_v = sdesc_sw128(sb + OFF_RING + (pv_g % kNS) * kSlot, kKChunk, 1024);
+          umma_ss(tmem, d_p, d_v, idesc_pv, first ? 0u : 1u);
+          umma_ss(tmem, d_p + 2, d_v + 128, idesc_pv, 1u);
+          umma_ss(tmem, d_p + 4, d_v + 256, idesc_pv, 1u);
+          umma_ss(tmem, d_p + 6, d_v + 384, idesc_pv, 1u);
+          umma_commit(bar(B_PEMPTY));
+          umma_commit(bar(B_EMPTY + pv_g % kNS));
+          ++pv_g;
+          progressed = true;
+        }
+      }
+      if (!have && pv_g == qk_g) break;
+      if (progressed) {
+        t_last = globaltimer();
+      } else {
+        if (*abort_flag) { failed = true; break; }
+        if (globaltimer() - t_last > guard.limit_ns) {
+          *abort_flag = 1u;
+          atomicOr(p.status, STATUS_TIMEOUT);
           failed = true;
           break;
         }
-        pend_g = g;
-        pend_first = (t == t0);
-        pend_piece = piece;
       }
-      ++piece;
     }
-    if (!failed && pend_g >= 0) issue_pv(pend_g, pend_first, pend_piece);
+    (void)failed;
     // every UMMA issued above has completed before TMEM is released
     umma_commit(bar(B_DRAIN));
     const uint64_t t_0 = globaltimer();
@@ -268,58 +340,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------- softmax / exchange / epilogue ----------------
     const int h = threadIdx.x - 128;                      // head = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
-    const uint32_t x_local = sb + OFF_SX + h * 256;
-    const uint32_t x_remote = mapa(x_local, peer);
+    const uint32_t xr_row = sb + OFF_XR + h * 256;        // same offset in both CTAs
+    const uint32_t xs_row = sb + OFF_XS + h * 256;
+    const uint32_t xr_remote = mapa(sb + OFF_XR, peer);
     const uint32_t xfull_remote = mapa(bar(B_XFULL), peer);
     const uint32_t xempty_remote = mapa(bar(B_XEMPTY), peer);
     const uint32_t p_row = sb + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
     const float sl2 = p.scale_log2;
-    PieceIter it(p, part);
-    int v, t0, t1, len, split;
-    bool fin;
-    int g = 0;
-    bool failed = false;
-    while (!failed && it.next(v, t0, t1, len, split, fin)) {
-      const int b = v % p.batch, i = v / p.batch;
-      float m = -INFINITY, l = 0.f;
-      for (int t = t0; t < t1; ++t, ++g) {
-        const int sbuf = g & 1;
-        uint32_t sr[64];
-        if (!__all_sync(0xffffffffu, wait(bar(B_SFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
-        tc_fence_after();
-        tmem_ld32(tl + kColS + 64u * sbuf, sr);
-        tmem_ld32(tl + kColS + 64u * sbuf + 32u, sr + 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(B_SEMPTY + sbuf));
-        // send my partial scores to the peer, receive and add the peer's
-        if (!__all_sync(0xffffffffu, wait_cluster(bar(B_XEMPTY), (g & 1) ^ 1, guard))) { failed = true; break; }
+
+    // copy this CTA's 256 latent dims of every head's query row into TMEM
+    auto load_q = [&](const Piece& q_pc, int q_idx) -> bool {
+      if (q_idx > 0 && !warp_ok(wait(bar(B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
+      const int b = q_pc.v % p.batch, i = q_pc.v / p.batch;
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
+                                                        ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank);
+      uint32_t r[128];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          st_cluster_v4(x_remote + ((u ^ (h & 7)) << 4), __uint_as_float(sr[4 * u]), __uint_as_float(sr[4 * u + 1]),
-                        __uint_as_float(sr[4 * u + 2]), __uint_as_float(sr[4 * u + 3]));
-        mbar_arrive_remote(xfull_remote);
-        if (!__all_sync(0xffffffffu, wait_cluster(bar(B_XFULL), g & 1, guard))) { failed = true; break; }
+      for (int k = 0; k < 32; ++k) {
+        const uint4 x = __ldg(src + k);
+        r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
+      }
+      tc_fence_after();
+      tmem_st32x4(tl + kColQ, r);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_QFULL));
+      return true;
+    };
+    // read S of tile gg from TMEM into `sr`, stage it, and copy it to the peer
+    auto send_partial = [&](int gg, uint32_t* sr) -> bool {
+      const int sbuf = gg & 1;
+      if (!warp_ok(wait(bar(B_SFULL + sbuf), (gg >> 1) & 1, guard))) return false;
+      tc_fence_after();
+      tmem_ld32(tl + kColS + 64u * sbuf, sr);
+      tmem_ld32(tl + kColS + 64u * sbuf + 32u, sr + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_SEMPTY + sbuf));
+      // the peer has consumed the previous message: the staging buffer and its
+      // receive buffer are free
+      if (!warp_ok(wait_cluster(bar(B_XEMPTY), (gg & 1) ^ 1, guard))) return false;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        st_shared_v4(xs_row + ((u ^ (h & 7)) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2], sr[4 * u + 3]);
+      fence_proxy_async_smem();
+      named_sync(kSoftmaxBar, 128);
+      if (h == 0) bulk_copy_to_peer(xr_remote, sb + OFF_XS, kXBytes, xfull_remote);
+      return true;
+    };
+
+    PieceIter it(p, part);
+    Piece pc, nx;
+    int g = 0, qi = 0;
+    bool failed = false;
+    bool have = it.next(pc);
+    if (have) failed = !load_q(pc, qi++);
+    uint32_t cur[64];
+    while (have && !failed) {
+      const int b = pc.v % p.batch, i = pc.v / p.batch;
+      float m = -INFINITY, l = 0.f;
+      if (!send_partial(g, cur)) { failed = true; break; }
+      for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+        // (1) receive the peer's partial of tile g and add it
+        if (h == 0) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
+        if (!warp_ok(wait_cluster(bar(B_XFULL), g & 1, guard))) { failed = true; break; }
         float s[64];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float4 o = ld_shared_v4f(x_local + ((u ^ (h & 7)) << 4));
-          s[4 * u + 0] = __uint_as_float(sr[4 * u + 0]) + o.x;
-          s[4 * u + 1] = __uint_as_float(sr[4 * u + 1]) + o.y;
-          s[4 * u + 2] = __uint_as_float(sr[4 * u + 2]) + o.z;
-          s[4 * u + 3] = __uint_as_float(sr[4 * u + 3]) + o.w;
+          const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
+          s[4 * u + 0] = __uint_as_float(cur[4 * u + 0]) + o.x;
+          s[4 * u + 1] = __uint_as_float(cur[4 * u + 1]) + o.y;
+          s[4 * u + 2] = __uint_as_float(cur[4 * u + 2]) + o.z;
+          s[4 * u + 3] = __uint_as_float(cur[4 * u + 3]) + o.w;
         }
-        mbar_arrive_remote(xempty_remote);
-        // valid tokens of this tile (a bad page masks the whole tile)
-        int nv = len - t * kTile;
-        nv = nv > kTile ? kTile : nv;
-        {
-          const int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-          if (page < 0 || page >= p.num_blocks) {
-            if (h == 0 && rank == 0) atomicOr(p.status, STATUS_INDEX);
-            nv = 0;
-          }
-        }
+        // the loads above have returned their values, so a relaxed arrive is
+        // enough to let the peer overwrite the buffer
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote);
+        // (2) send the partial of tile g+1 (same piece)
+        if (t + 1 < pc.t1 && !send_partial(g + 1, cur)) { failed = true; break; }
+        // (3) softmax of tile g
+        const int nv = dense_valid(p, b, t, pc.len, h == 0 && rank == 0);
         float mt = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 64; ++k) {
@@ -328,23 +429,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const float m_new = fmaxf(m, mt);
         // lazy rescale: keep the old reference max unless the new one is
-        // more than 2^8 larger (P stays <= 256, exact in the accumulation)
+        // more than 2^8 larger (P stays <= 256)
         const bool resc = m_new > m + 8.0f;
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? exp2_approx(m - m_new) : 1.0f;
         const float m_ref = m_use == -INFINITY ? 0.f : m_use;
-        float rs = 0.f;
+        float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < 64; k += 2) {
           s[k] = exp2_approx(s[k] - m_ref);
-          rs += s[k];
+          s[k + 1] = exp2_approx(s[k + 1] - m_ref);
+          rs0 += s[k];
+          rs1 += s[k + 1];
         }
-        l = l * alpha + rs;
+        l = l * alpha + (rs0 + rs1);
         m = m_use;
         // the previous P . V has finished: P buffer and O are free
-        if (g > 0 && !__all_sync(0xffffffffu, wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
+        if (g > 0 && !warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
         tc_fence_after();
-        if (resc && t != t0) {
+        if (resc && t != pc.t0) {
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
             uint32_t r[32];
@@ -379,8 +482,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(B_PFULL));
       }
       if (failed) break;
+      // the next piece's Q goes into TMEM before this piece's epilogue, so
+      // its first QK^T overlaps the epilogue
+      const bool have_next = it.next(nx);
+      if (have_next && !load_q(nx, qi++)) { failed = true; break; }
       // ---- epilogue of the piece: O / l -> out (single piece) or partial ----
-      if (!__all_sync(0xffffffffu, wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
+      if (!warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -390,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tl + 32u * c, r);
         tmem_wait_ld();
-        if (fin) {
+        if (pc.fin) {
           OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + 32 * c;
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
@@ -403,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + k) = w;
           }
         } else {
-          float* dst = p.o_part + ((int64_t)split * 128 + h) * kDV + 256 * rank + 32 * c;
+          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * c;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<float4*>(dst + k) =
@@ -412,11 +519,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (rank == 0) {
-        if (fin) p.lse[row] = lse;
-        else p.lse_part[(int64_t)split * 128 + h] = lse;
+        if (pc.fin) p.lse[row] = lse;
+        else p.lse_part[(int64_t)pc.split * 128 + h] = lse;
       }
       tc_fence_before();
       mbar_arrive(bar(B_OEMPTY));
+      pc = nx;
+      have = have_next;
     }
   }
 

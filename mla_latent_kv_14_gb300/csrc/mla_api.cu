@@ -192,16 +192,19 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
 
   const bool fp16 = q_dtype == MLA_DTYPE_FP16;
   const CUtensorMapDataType dt = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap tm_q, tm_kv;
-  if (!make_map(&tm_q, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return MLA_ERR_CUDA;
-  if (!make_map(&tm_kv, kvcache, dt, 2, (uint64_t)(num_blocks * page_block), kDK, kDK * 2, 64, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+  // Q: the 32-dim RoPE halves (64-B swizzle); KV: 64-dim latent chunks
+  // (128-B swizzle) and 32-dim RoPE halves (64-B swizzle)
+  CUtensorMap tm_qr, tm_kv, tm_kvr;
+  const uint64_t kvrows = (uint64_t)(num_blocks * page_block);
+  if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&tm_kv, kvcache, dt, 2, kvrows, kDK, kDK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&tm_kvr, kvcache, dt, 2, kvrows, kDK, kDK * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
 
   const int64_t S = max_splits(batch * s_q, parts);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeParams p{};
+  p.q = q;
   p.block_table = block_table;
   p.seqlens = cache_seqlens;
   p.indices = indices;
@@ -233,9 +236,9 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     cfg.dynamicSmemBytes = dense::kSmemBytes;
     cfg.stream = st;
     if (fp16)
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<true>, tm_q, tm_kv, p));
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<true>, tm_qr, tm_kv, tm_kvr, p));
     else
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<false>, tm_q, tm_kv, p));
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<false>, tm_qr, tm_kv, tm_kvr, p));
   }
   if (!(stages & STAGE_COMBINE)) return MLA_OK;
 

@@ -48,6 +48,7 @@ struct MetaParams {
 };
 
 struct DecodeParams {
+  const void* q;               // [batch, s_q, h_q, 576]
   const int32_t* block_table;  // [batch, max_blocks] (dense)
   const int32_t* seqlens;      // [batch]
   const int32_t* indices;      // [batch, s_q, topk] (sparse) or null
