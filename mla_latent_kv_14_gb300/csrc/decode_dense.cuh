@@ -15,12 +15,16 @@
 // cluster split the latent dimension: CTA r keeps O[:, 256r : 256r+256] in TMEM
 // (256 columns) and loads only its own part of Q and of every KV tile: CTA r
 // the latent dims [256r, 256r+256) and the RoPE dims [512+32r, 544+32r).
-// Each CTA computes a partial S over its dims with single-CTA
-// UMMA (M=128 heads, N=64 tokens); the two fp32 partials are exchanged through
-// distributed shared memory and summed, so both CTAs hold the full S, run the
-// same softmax (bit-identical), and accumulate P . V for their own half of the
-// latent (M=128, N=256, K=64). No tensor-core work is duplicated and no KV byte
-// is read twice. (Prior art on the pages: the Hopper kernel splits O between
+// Each CTA computes a partial score S_r over its dims with single-CTA UMMA
+// (M=128 heads, N=64 tokens). Instead of exchanging S_r, each CTA exponentiates
+// it, E_r = exp2((S_r - m_r) * scale*log2e) with m_r its partial row max, and
+// sends E_r (in [0,1]) as fp16 plus m_r: exp(S_0 + S_1 - m) = E_0 * E_1 *
+// exp(m_0 + m_1 - m) is exact algebra, so both CTAs form the same P = E_0 *
+// E_1 * 2^(m_0 + m_1 - m_ref) (identical fp16 operands, commutative products;
+// a factor below 2^-24 flushes to 0) and accumulate P . V
+// for their own half of the latent (M=128, N=256, K=64). No tensor-core work is
+// duplicated and no KV byte is read twice; the exchange is 16.5 KB per tile
+// and direction. (Prior art on the pages: the Hopper kernel splits O between
 // two warpgroups -- seesaw -- because the register file is full, and the FP8
 // kernel pairs two CTAs over DSM -- Crossover; here the pair exists because
 // TMEM is full.)
@@ -28,27 +32,28 @@
 // Memory map. TMEM (512 columns): O half [0,256), S buffers [256,320) and
 // [320,384), and this CTA's 256 latent dims of Q as the UMMA A operand
 // [384,512) (column j = bf16 pair (2j, 2j+1) of head row = lane). Shared
-// memory: the peer's partial scores (fp32, 32 KB), this CTA's partial scores
-// staged for the copy to the peer (32 KB), P (bf16, 16 KB), the CTA's 32 RoPE
-// dims of Q (8 KB) and a 3-slot ring of KV tiles (36 KB each: four 64-wide
-// latent chunks, 128-byte swizzled, and one 32-wide RoPE chunk, 64-byte
-// swizzled, of 64 tokens). The producer also prefetches the tiles beyond the
-// ring into L2.
+// memory: the peer's message and this CTA's staged message (E_r fp16 128x64 +
+// m_r, 17 KB each), P (bf16, 16 KB), the CTA's 32 RoPE dims of Q (8 KB) and a
+// 4-slot ring of KV tiles (36 KB each: four 64-wide latent chunks, 128-byte
+// swizzled, and one 32-wide RoPE chunk, 64-byte swizzled, of 64 tokens). The
+// producer also prefetches the tiles beyond the ring into L2.
 //
-// Warp roles (256 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM
-// and lane 0 issues UMMA; warps 4-7 are the softmax / exchange / epilogue
-// warps, thread h <-> TMEM lane h <-> head h; they also copy each piece's Q
-// rows into TMEM. Warps 2-3 only take part in set-up and tear-down.
+// Warp roles (384 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM
+// and lane 0 issues UMMA; warps 4-11 are the softmax / exchange / epilogue
+// warps: warp w serves TMEM lanes (heads) 32*(w%4) .. +31 and the score
+// columns (tokens) [32c, 32c+32) with c = (w-4)/4, so two warps share each
+// head row (the row max is combined through shared memory; the running sums
+// stay per half until the epilogue). They also copy each piece's Q rows into
+// TMEM. Warps 2-3 only take part in set-up and tear-down.
 //
-// Pipeline. The exchange of a tile's partial scores is one bulk shared-to-
-// shared copy into the peer (the bytes complete on the peer's mbarrier); the
-// buffer-free signal is one remote arrive per warp. The softmax loop runs
-// "receive tile g, send tile g+1, softmax of tile g", so each exchange is in
-// flight while the other tile's math runs. The UMMA issuer polls its inputs
-// and issues whichever of QK^T / P.V is ready, so neither waits behind the
-// other. Measured on GB300: DSM moves about 18 B/clk per SM,
-// and small single-CTA UMMAs cost 50-70 cycles each to issue, so these two,
-// not the shared-memory ring, bound the tile rate.
+// Pipeline. A tile's message is one bulk shared-to-shared copy into the peer
+// (the bytes complete on the peer's mbarrier); the buffer-free signal is one
+// remote arrive per warp. The softmax loop runs "receive tile g, exponentiate
+// and send tile g+1, form P of tile g", so each exchange is in flight while the
+// other tile's work runs. The UMMA issuer polls its inputs and issues whichever
+// of QK^T / P.V is ready. Measured on GB300: DSM bulk copies move about 9-18
+// B/clk per SM under load and small single-CTA UMMAs cost 50-70 cycles each to
+// issue; these bound the tile rate.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -60,31 +65,36 @@
 namespace mla {
 namespace dense {
 
-constexpr int kNS = 3;                     // KV ring slots (tiles)
+constexpr int kNS = 4;                     // KV ring slots (tiles)
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
 constexpr int kSlot = 4 * kKChunk + kRChunk;
 constexpr int kPrefetch = kNS;             // tiles ahead of the ring prefetched into L2
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
 constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
-constexpr uint32_t kXBytes = 128 * 256;    // one partial-score message
+constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
+constexpr uint32_t kXBytes = kXE + 128 * 4;             // + m_r per row
+constexpr uint32_t kXStride = 17 * 1024;
 
 // shared memory map (offsets from a 1024-B aligned base)
-constexpr uint32_t OFF_XR = 0;                          // peer's partial: 128 rows x 64 fp32
-constexpr uint32_t OFF_XS = OFF_XR + kXBytes;           // own partial, staged for the copy
-constexpr uint32_t OFF_P = OFF_XS + kXBytes;            // 128 rows x 64 bf16
+constexpr uint32_t OFF_XR = 0;                          // peer's message
+constexpr uint32_t OFF_XS = OFF_XR + kXStride;          // own message, staged for the copy
+constexpr uint32_t OFF_P = OFF_XS + kXStride;           // 128 rows x 64 bf16
 constexpr uint32_t OFF_QR = OFF_P + 128 * 128;          // 32 RoPE dims of Q: 128 rows x 64 B
 constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
-constexpr uint32_t OFF_BAR = OFF_RING + kNS * kSlot;
+constexpr uint32_t OFF_MX = OFF_RING + kNS * kSlot;     // row-max halves [2 tiles][2 halves][128], l halves [2][128]
+constexpr uint32_t OFF_BAR = OFF_MX + 3 * 2 * 128 * 4;
 enum : uint32_t {
   B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY, B_SFULL, B_SEMPTY = B_SFULL + 2,
   B_PFULL = B_SEMPTY + 2, B_PEMPTY, B_OEMPTY, B_XFULL, B_XEMPTY, B_DRAIN, B_COUNT
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;    // tmem slot, abort flag, ok flag
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
-constexpr uint32_t kSoftmaxBar = 1;                     // named barrier of the 128 softmax threads
+constexpr uint32_t kSoftmaxBar = 1;                     // named barrier of the 256 softmax threads
+constexpr uint32_t kPairBar = 2;                        // + quadrant: the two warps of one lane quadrant
 
 
 // iteration over the pieces of one SM part (every role walks the same list)
@@ -163,17 +173,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_QFULL), 128 + 1);  // softmax threads (latent into TMEM) + RoPE TMA
+    mbar_init(bar(B_QFULL), kSoftmaxWarps + 1);  // softmax warps (latent into TMEM) + RoPE TMA
     mbar_init(bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 128);
+      mbar_init(bar(B_SEMPTY + s), kSoftmaxWarps);
     }
-    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_PFULL), kSoftmaxWarps);
     mbar_init(bar(B_PEMPTY), 1);
-    mbar_init(bar(B_OEMPTY), 128);
+    mbar_init(bar(B_OEMPTY), kSoftmaxWarps);
     mbar_init(bar(B_XFULL), 1);    // own expect_tx + the peer's copied bytes
-    mbar_init(bar(B_XEMPTY), 4);   // one arrive per peer softmax warp
+    mbar_init(bar(B_XEMPTY), kSoftmaxWarps);  // one arrive per peer softmax warp
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0u;
     *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
@@ -338,54 +348,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t_0 < 200000000ull) {}
   } else if (ok && warp >= 4) {
     // ---------------- softmax / exchange / epilogue ----------------
-    const int h = threadIdx.x - 128;                      // head = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
-    const uint32_t xr_row = sb + OFF_XR + h * 256;        // same offset in both CTAs
-    const uint32_t xs_row = sb + OFF_XS + h * 256;
+    const int q4 = warp & 3;                              // TMEM lane quadrant
+    const int c = (warp - 4) >> 2;                        // score column half
+    const int h = 32 * q4 + lane;                         // head = TMEM lane
+    const int sid = threadIdx.x - 128;                    // 0..255 among softmax threads
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t xr_row = sb + OFF_XR + h * 128;        // same offsets in both CTAs
+    const uint32_t xs_row = sb + OFF_XS + h * 128;
     const uint32_t xr_remote = mapa(sb + OFF_XR, peer);
     const uint32_t xfull_remote = mapa(bar(B_XFULL), peer);
     const uint32_t xempty_remote = mapa(bar(B_XEMPTY), peer);
     const uint32_t p_row = sb + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
+    float* mx = reinterpret_cast<float*>(smem + OFF_MX);  // [tile parity][half][row]
+    float* lx = mx + 2 * 256;                             // [half][row]
+    const float* xr_m = reinterpret_cast<const float*>(smem + OFF_XR + kXE);
+    float* xs_m = reinterpret_cast<float*>(smem + OFF_XS + kXE);
     const float sl2 = p.scale_log2;
+    const uint32_t pair_bar = kPairBar + q4;
 
     // copy this CTA's 256 latent dims of every head's query row into TMEM
+    // (each of the two warps of a quadrant copies 128 of them)
     auto load_q = [&](const Piece& q_pc, int q_idx) -> bool {
       if (q_idx > 0 && !warp_ok(wait(bar(B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
       const int b = q_pc.v % p.batch, i = q_pc.v / p.batch;
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
-                                                        ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank);
-      uint32_t r[128];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint16_t*>(p.q) + ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank + 128 * c);
+      uint32_t r[64];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const uint4 x = __ldg(src + k);
         r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
       }
       tc_fence_after();
-      tmem_st32x4(tl + kColQ, r);
+      tmem_st32(tl + kColQ + 64u * c, r);
+      tmem_st32(tl + kColQ + 64u * c + 32u, r + 32);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_QFULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QFULL));
       return true;
     };
-    // read S of tile gg from TMEM into `sr`, stage it, and copy it to the peer
-    auto send_partial = [&](int gg, uint32_t* sr) -> bool {
+    // Tile gg: read this warp's 32 partial-score columns from TMEM, E_r =
+    // exp2(x - m_r) with x = S_r * scale * log2e and m_r the partial row max
+    // over the nvg valid tokens (masked tokens get E = 0), kept as fp16 pairs
+    // in `e`; stage E_r and m_r and copy them to the peer.
+    auto send_partial = [&](int gg, int nvg, uint32_t* e, float& m_own) -> bool {
       const int sbuf = gg & 1;
       if (!warp_ok(wait(bar(B_SFULL + sbuf), (gg >> 1) & 1, guard))) return false;
       tc_fence_after();
-      tmem_ld32(tl + kColS + 64u * sbuf, sr);
-      tmem_ld32(tl + kColS + 64u * sbuf + 32u, sr + 32);
+      uint32_t sr[32];
+      tmem_ld32(tl + kColS + 64u * sbuf + 32u * c, sr);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY + sbuf));
-      // the peer has consumed the previous message: the staging buffer and its
-      // receive buffer are free
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sbuf));
+      const int nvc = nvg - 32 * c;  // valid columns in this half
+      float x[32];
+      float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        x[k] = k < nvc ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
+        x[k + 1] = k + 1 < nvc ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
+        m0 = fmaxf(m0, x[k]);
+        m1 = fmaxf(m1, x[k + 1]);
+      }
+      float* mxg = mx + (gg & 1) * 256;
+      mxg[c * 128 + h] = fmaxf(m0, m1);
+      named_sync(pair_bar, 64);
+      m_own = fmaxf(mxg[h], mxg[128 + h]);
+      const float mref = m_own == -INFINITY ? 0.f : m_own;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) e[u] = pack_f16x2(exp2_approx(x[2 * u] - mref), exp2_approx(x[2 * u + 1] - mref));
+      // the peer has consumed the previous message: staging and its receive
+      // buffer are free
       if (!warp_ok(wait_cluster(bar(B_XEMPTY), (gg & 1) ^ 1, guard))) return false;
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        st_shared_v4(xs_row + ((u ^ (h & 7)) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2], sr[4 * u + 3]);
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(xs_row + (((4 * c + u) ^ (h & 7)) << 4), e[4 * u], e[4 * u + 1], e[4 * u + 2], e[4 * u + 3]);
+      if (c == 0) xs_m[h] = m_own;
       fence_proxy_async_smem();
-      named_sync(kSoftmaxBar, 128);
-      if (h == 0) bulk_copy_to_peer(xr_remote, sb + OFF_XS, kXBytes, xfull_remote);
+      named_sync(kSoftmaxBar, 256);
+      if (sid == 0) bulk_copy_to_peer(xr_remote, sb + OFF_XS, kXBytes, xfull_remote);
       return true;
     };
 
@@ -395,67 +438,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool failed = false;
     bool have = it.next(pc);
     if (have) failed = !load_q(pc, qi++);
-    uint32_t cur[64];
+    uint32_t cur[16];   // own E of the tile being finished (fp16 pairs)
+    float m_cur = -INFINITY;
     while (have && !failed) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
-      float m = -INFINITY, l = 0.f;
-      if (!send_partial(g, cur)) { failed = true; break; }
+      float m = -INFINITY, l_half = 0.f;
+      int nv_cur = dense_valid(p, b, pc.t0, pc.len, false);
+      if (!send_partial(g, nv_cur, cur, m_cur)) { failed = true; break; }
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        // (1) receive the peer's partial of tile g and add it
-        if (h == 0) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
+        const int nv = nv_cur;
+        if (nv == 0 && sid == 0 && rank == 0) atomicOr(p.status, STATUS_INDEX);  // unreachable page
+        // (1) receive the peer's E and m of tile g
+        if (sid == 0) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
         if (!warp_ok(wait_cluster(bar(B_XFULL), g & 1, guard))) { failed = true; break; }
-        float s[64];
+        uint32_t ep[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
-          s[4 * u + 0] = __uint_as_float(cur[4 * u + 0]) + o.x;
-          s[4 * u + 1] = __uint_as_float(cur[4 * u + 1]) + o.y;
-          s[4 * u + 2] = __uint_as_float(cur[4 * u + 2]) + o.z;
-          s[4 * u + 3] = __uint_as_float(cur[4 * u + 3]) + o.w;
+        for (int u = 0; u < 4; ++u) {
+          const float4 o = ld_shared_v4f(xr_row + (((4 * c + u) ^ (h & 7)) << 4));
+          ep[4 * u] = __float_as_uint(o.x); ep[4 * u + 1] = __float_as_uint(o.y);
+          ep[4 * u + 2] = __float_as_uint(o.z); ep[4 * u + 3] = __float_as_uint(o.w);
         }
+        const float m_peer = xr_m[h];
         // the loads above have returned their values, so a relaxed arrive is
         // enough to let the peer overwrite the buffer
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote);
-        // (2) send the partial of tile g+1 (same piece)
-        if (t + 1 < pc.t1 && !send_partial(g + 1, cur)) { failed = true; break; }
-        // (3) softmax of tile g
-        const int nv = dense_valid(p, b, t, pc.len, h == 0 && rank == 0);
-        float mt = -INFINITY;
+        uint32_t eo[16];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] = k < nv ? s[k] * sl2 : -INFINITY;
-          mt = fmaxf(mt, s[k]);
+        for (int u = 0; u < 16; ++u) eo[u] = cur[u];
+        const float m_mine = m_cur;
+        // (2) exponentiate and send tile g+1 (same piece)
+        if (t + 1 < pc.t1) {
+          nv_cur = dense_valid(p, b, t + 1, pc.len, false);
+          if (!send_partial(g + 1, nv_cur, cur, m_cur)) { failed = true; break; }
         }
+        // (3) P of tile g: E_0 * E_1 * 2^(m_0 + m_1 - m_ref), lazy rescale
+        // against the running reference max (P stays <= 256)
+        const float mt = m_mine + m_peer;  // upper bound of the tile's scaled row max
         const float m_new = fmaxf(m, mt);
-        // lazy rescale: keep the old reference max unless the new one is
-        // more than 2^8 larger (P stays <= 256)
         const bool resc = m_new > m + 8.0f;
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? exp2_approx(m - m_new) : 1.0f;
-        const float m_ref = m_use == -INFINITY ? 0.f : m_use;
+        const float cf = mt == -INFINITY ? 0.f : exp2_approx(mt - (m_use == -INFINITY ? 0.f : m_use));
         float rs0 = 0.f, rs1 = 0.f;
+        uint32_t pw[16];
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          s[k] = exp2_approx(s[k] - m_ref);
-          s[k + 1] = exp2_approx(s[k + 1] - m_ref);
-          rs0 += s[k];
-          rs1 += s[k + 1];
+        for (int u = 0; u < 16; ++u) {
+          const float2 fo = unpack_f16x2(eo[u]), fq = unpack_f16x2(ep[u]);
+          const float a0 = fo.x * fq.x * cf;
+          const float a1 = fo.y * fq.y * cf;
+          rs0 += a0;
+          rs1 += a1;
+          pw[u] = kFp16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
         }
-        l = l * alpha + (rs0 + rs1);
+        l_half = l_half * alpha + (rs0 + rs1);
         m = m_use;
         // the previous P . V has finished: P buffer and O are free
         if (g > 0 && !warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
         tc_fence_after();
-        if (resc && t != pc.t0) {
+        if (__any_sync(0xffffffffu, resc) && t != pc.t0) {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t r[32];
-            tmem_ld32(tl + 32u * c, r);
+            const uint32_t col = 128u * c + 32u * cc;
+            tmem_ld32(tl + col, r);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-            tmem_st32(tl + 32u * c, r);
+            tmem_st32(tl + col, r);
           }
           tmem_wait_st();
         }
@@ -463,23 +513,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
           // turn into NaN inside P . V
           const uint32_t slot = sb + OFF_RING + (g % kNS) * kSlot;
-          const int nrow = (kTile - nv) * 4;  // rows x 4 V chunks
-          for (int e = h; e < nrow * 8; e += 128) {
-            const int rr = e >> 3, ch = rr / (kTile - nv), row = nv + rr % (kTile - nv);
-            st_shared_v4(slot + ch * kKChunk + row * 128 + (e & 7) * 16, 0u, 0u, 0u, 0u);
+          const int nz = kTile - (nv > 0 ? nv : 0);
+          const int nrow = nz * 4;  // rows x 4 V chunks
+          for (int e2 = sid; e2 < nrow * 8; e2 += 256) {
+            const int rr = e2 >> 3, ch = rr / nz, row = kTile - nz + rr % nz;
+            st_shared_v4(slot + ch * kKChunk + row * 128 + (e2 & 7) * 16, 0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t w0 = kFp16 ? pack_f16x2(s[8 * u + 0], s[8 * u + 1]) : pack_bf16x2(s[8 * u + 0], s[8 * u + 1]);
-          const uint32_t w1 = kFp16 ? pack_f16x2(s[8 * u + 2], s[8 * u + 3]) : pack_bf16x2(s[8 * u + 2], s[8 * u + 3]);
-          const uint32_t w2 = kFp16 ? pack_f16x2(s[8 * u + 4], s[8 * u + 5]) : pack_bf16x2(s[8 * u + 4], s[8 * u + 5]);
-          const uint32_t w3 = kFp16 ? pack_f16x2(s[8 * u + 6], s[8 * u + 7]) : pack_bf16x2(s[8 * u + 6], s[8 * u + 7]);
-          st_shared_v4(p_row + ((u ^ (h & 7)) << 4), w0, w1, w2, w3);
-        }
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(p_row + (((4 * c + u) ^ (h & 7)) << 4), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL));
       }
       if (failed) break;
       // the next piece's Q goes into TMEM before this piece's epilogue, so
@@ -487,18 +534,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool have_next = it.next(nx);
       if (have_next && !load_q(nx, qi++)) { failed = true; break; }
       // ---- epilogue of the piece: O / l -> out (single piece) or partial ----
+      lx[c * 128 + h] = l_half;
+      named_sync(pair_bar, 64);
+      const float l = lx[h] + lx[128 + h];
       if (!warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       const int64_t row = (int64_t)(b * p.s_q + i) * 128 + h;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
-        tmem_ld32(tl + 32u * c, r);
+        const int col = 128 * c + 32 * cc;
+        tmem_ld32(tl + (uint32_t)col, r);
         tmem_wait_ld();
         if (pc.fin) {
-          OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + 32 * c;
+          OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + col;
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
             uint4 w;
@@ -510,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + k) = w;
           }
         } else {
-          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * c;
+          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + col;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<float4*>(dst + k) =
@@ -518,12 +569,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             __uint_as_float(r[k + 2]) * inv_l, __uint_as_float(r[k + 3]) * inv_l);
         }
       }
-      if (rank == 0) {
+      if (rank == 0 && c == 0) {
         if (pc.fin) p.lse[row] = lse;
         else p.lse_part[(int64_t)pc.split * 128 + h] = lse;
       }
       tc_fence_before();
-      mbar_arrive(bar(B_OEMPTY));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_OEMPTY));
       pc = nx;
       have = have_next;
     }
