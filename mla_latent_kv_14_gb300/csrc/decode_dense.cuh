@@ -65,37 +65,55 @@
 namespace mla {
 namespace dense {
 
-constexpr int kNS = 4;                     // KV ring slots (tiles)
+enum : int { MODE_BF16 = 0, MODE_FP16 = 1, MODE_FP8 = 2, MODE_FP8_SPARSE = 3 };
+
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
 constexpr int kSlot = 4 * kKChunk + kRChunk;
-constexpr int kPrefetch = kNS;             // tiles ahead of the ring prefetched into L2
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
+constexpr int kDequantWarps = 2;           // warps 2-3 (FP8 caches)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
 constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
 constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
 constexpr uint32_t kXBytes = kXE + 128 * 4;             // + m_r per row
 constexpr uint32_t kXStride = 17 * 1024;
-
-// shared memory map (offsets from a 1024-B aligned base)
-constexpr uint32_t OFF_XR = 0;                          // peer's message
-constexpr uint32_t OFF_XS = OFF_XR + kXStride;          // own message, staged for the copy
-constexpr uint32_t OFF_P = OFF_XS + kXStride;           // 128 rows x 64 bf16
-constexpr uint32_t OFF_QR = OFF_P + 128 * 128;          // 32 RoPE dims of Q: 128 rows x 64 B
-constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
-constexpr uint32_t OFF_MX = OFF_RING + kNS * kSlot;     // row-max halves [2 tiles][2 halves][128], l halves [2][128]
-constexpr uint32_t OFF_BAR = OFF_MX + 3 * 2 * 128 * 4;
-enum : uint32_t {
-  B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY, B_SFULL, B_SEMPTY = B_SFULL + 2,
-  B_PFULL = B_SEMPTY + 2, B_PEMPTY, B_OEMPTY, B_XFULL, B_XEMPTY, B_DRAIN, B_COUNT
-};
-constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;    // tmem slot, abort flag, ok flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;   // + alignment slack
 constexpr uint32_t kSoftmaxBar = 1;                     // named barrier of the 256 softmax threads
 constexpr uint32_t kPairBar = 2;                        // + quadrant: the two warps of one lane quadrant
+// FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
+constexpr uint32_t kRawLat = 64 * 256;     // this CTA's 256 e4m3 per token
+constexpr uint32_t kRawSc = 64 * 16;       // the 4 scales per token
+constexpr uint32_t kRawRope = 64 * 64;     // this CTA's 32 RoPE dims per token (sparse staging)
+constexpr uint32_t kRawSlot = kRawLat + kRawSc + kRawRope;
+constexpr int kRawNS = 2;
 
+// per-mode layout (offsets from a 1024-B aligned base) and barrier indices
+template <int kMode>
+struct Cfg {
+  static constexpr bool kFp16 = kMode == MODE_FP16;
+  static constexpr bool kFp8 = kMode >= MODE_FP8;
+  static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
+  static constexpr int kNS = kFp8 ? 3 : 4;               // KV ring slots (tiles)
+  static constexpr int kPrefetch = kNS;                  // dense: tiles ahead of the ring prefetched into L2
+  static constexpr uint32_t OFF_XR = 0;                  // peer's message
+  static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
+  static constexpr uint32_t OFF_P = OFF_XS + kXStride;   // 128 rows x 64 bf16
+  static constexpr uint32_t OFF_QR = OFF_P + 128 * 128;  // 32 RoPE dims of Q: 128 rows x 64 B
+  static constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
+  static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlot;
+  static constexpr uint32_t OFF_MX = OFF_RAW + (kFp8 ? kRawNS * kRawSlot : 0);  // row max / row sum halves
+  static constexpr uint32_t OFF_BAR = OFF_MX + 3 * 2 * 128 * 4;
+  static constexpr uint32_t B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1,
+                            B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2,
+                            B_PEMPTY = B_PFULL + 1, B_OEMPTY = B_PEMPTY + 1, B_XFULL = B_OEMPTY + 1,
+                            B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_RFULL = B_DRAIN + 1,
+                            B_REMPTY = B_RFULL + kRawNS, B_COUNT = B_REMPTY + kRawNS;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem slot, abort flag, ok flag
+  static constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;  // + alignment slack
+};
+static_assert(Cfg<MODE_BF16>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
 // iteration over the pieces of one SM part (every role walks the same list)
 struct Piece {
@@ -136,21 +154,57 @@ struct PieceIter {
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
 
 // valid tokens of tile t of a dense request (0 if its page is out of range)
-__device__ __forceinline__ int dense_valid(const DecodeParams& p, int b, int t, int len, bool report) {
+__device__ __forceinline__ int dense_valid(const DecodeParams& p, int b, int t, int len) {
   int nv = len - t * kTile;
   nv = nv > kTile ? kTile : nv;
   const int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-  if (page < 0 || page >= p.num_blocks) {
-    if (report) atomicOr(p.status, STATUS_INDEX);
-    nv = 0;
-  }
-  return nv;
+  return (page < 0 || page >= p.num_blocks) ? 0 : nv;
 }
 
-template <bool kFp16>
+// Validity of the 64 tokens of tile t as a bit mask (bit k = token 64t+k),
+// computed by a whole warp. Dense: the first nv tokens (a tile whose page is
+// out of range is empty). Sparse: the index-list entries in [0, num_rows);
+// -1 is silently skipped, other out-of-range entries are reported.
+template <bool kSparse>
+__device__ __forceinline__ uint64_t tile_mask(const DecodeParams& p, int v, int t, int len, bool report) {
+  const int lane = threadIdx.x & 31;
+  if constexpr (!kSparse) {
+    const int b = v % p.batch;
+    const int nv = dense_valid(p, b, t, len);
+    if (report && nv == 0 && lane == 0) atomicOr(p.status, STATUS_INDEX);
+    return nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+  } else {
+    const int b = v % p.batch, i = v / p.batch;
+    const int32_t* row = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
+    uint32_t half[2];
+    bool bad = false;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int k = 64 * t + 32 * hh + lane;
+      const int idx = k < p.topk ? __ldg(row + k) : -1;
+      const bool ok = idx >= 0 && (int64_t)idx < p.num_rows;
+      bad |= (idx != -1 && !ok);
+      half[hh] = __ballot_sync(0xffffffffu, ok);
+    }
+    if (report && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, STATUS_INDEX);
+    return (uint64_t)half[0] | ((uint64_t)half[1] << 32);
+  }
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_dense_kernel(const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_kv,
-                            const __grid_constant__ CUtensorMap tm_kvr, const DecodeParams p) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_kv,
+                      const __grid_constant__ CUtensorMap tm_kvr, const __grid_constant__ CUtensorMap tm_sc,
+                      const DecodeParams p) {
+  using C = Cfg<kMode>;
+  constexpr bool kFp16 = C::kFp16, kFp8 = C::kFp8, kSparse = C::kSparse;
+  constexpr int NS = C::kNS;
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,8 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int part = (int)cluster_id_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  auto bar = [&](uint32_t i) { return sb + OFF_BAR + 8u * i; };
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  auto bar = [&](uint32_t i) { return sb + C::OFF_BAR + 8u * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
   volatile uint32_t* ok_flag = misc + 2;
@@ -169,22 +223,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1);
+    for (int s = 0; s < NS; ++s) {
+      // producer (+ the two dequant warps for FP8 caches)
+      mbar_init(bar(C::B_FULL + s), kFp8 ? 1 + kDequantWarps : 1);
+      mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    mbar_init(bar(B_QFULL), kSoftmaxWarps + 1);  // softmax warps (latent into TMEM) + RoPE TMA
-    mbar_init(bar(B_QEMPTY), 1);
+    mbar_init(bar(C::B_QFULL), kSoftmaxWarps + 1);  // softmax warps (latent into TMEM) + RoPE TMA
+    mbar_init(bar(C::B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), kSoftmaxWarps);
+      mbar_init(bar(C::B_SFULL + s), 1);
+      mbar_init(bar(C::B_SEMPTY + s), kSoftmaxWarps);
     }
-    mbar_init(bar(B_PFULL), kSoftmaxWarps);
-    mbar_init(bar(B_PEMPTY), 1);
-    mbar_init(bar(B_OEMPTY), kSoftmaxWarps);
-    mbar_init(bar(B_XFULL), 1);    // own expect_tx + the peer's copied bytes
-    mbar_init(bar(B_XEMPTY), kSoftmaxWarps);  // one arrive per peer softmax warp
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(C::B_PFULL), kSoftmaxWarps);
+    mbar_init(bar(C::B_PEMPTY), 1);
+    mbar_init(bar(C::B_OEMPTY), kSoftmaxWarps);
+    mbar_init(bar(C::B_XFULL), 1);              // own expect_tx + the peer's copied bytes
+    mbar_init(bar(C::B_XEMPTY), kSoftmaxWarps);  // one arrive per peer softmax warp
+    mbar_init(bar(C::B_DRAIN), 1);
+    for (int s = 0; s < kRawNS; ++s) {
+      mbar_init(bar(C::B_RFULL + s), 1);
+      mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
+    }
     *abort_flag = 0u;
     *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
     if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
@@ -201,70 +260,213 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool ok = *ok_flag != 0u;
 
-  if (ok && warp == 0 && lane == 0) {
-    // ---------------- producer: RoPE dims of Q per piece, KV chunks per tile ----------------
-    prefetch_tmap(&tm_qr);
-    prefetch_tmap(&tm_kv);
-    prefetch_tmap(&tm_kvr);
+  if (ok && warp == 0 && (kSparse || lane == 0)) {
+    // ---------------- producer: RoPE dims of Q per piece, KV per tile ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tm_qr);
+      if constexpr (!kSparse) {
+        prefetch_tmap(&tm_kv);
+        prefetch_tmap(&tm_kvr);
+        if constexpr (kFp8) prefetch_tmap(&tm_sc);
+      }
+    }
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    const int xr = 512 + 32 * (int)rank;  // RoPE column of this CTA
+    const int xr = 512 + 32 * (int)rank;  // RoPE column of this CTA (bf16 caches)
     PieceIter it(p, part);
     Piece pc;
     int g = 0, qn = 0;
-    int last_g[kNS];
-    for (int s = 0; s < kNS; ++s) last_g[s] = -1;
+    int last_g[NS];
+    for (int s = 0; s < NS; ++s) last_g[s] = -1;
+    int last_rg[kRawNS] = {-1, -1};
     int q_last = -1;
     bool stop = false;
     auto page_of = [&](int b, int t) {
       int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-      return (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the softmax warps
+      return (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the consumers
     };
     auto prefetch_tile = [&](int page) {
+      if constexpr (kFp8) {
+        tma_prefetch_2d(&tm_kv, 256 * (int)rank, page * kTile);
+      } else {
 #pragma unroll
-      for (int ci = 0; ci < 4; ++ci) tma_prefetch_2d(&tm_kv, 256 * (int)rank + 64 * ci, page * kTile);
-      tma_prefetch_2d(&tm_kvr, xr, page * kTile);
+        for (int ci = 0; ci < 4; ++ci) tma_prefetch_2d(&tm_kv, 256 * (int)rank + 64 * ci, page * kTile);
+        tma_prefetch_2d(&tm_kvr, xr, page * kTile);
+      }
     };
     while (!stop && it.next(pc)) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
-      if (!wait(bar(B_QEMPTY), (qn & 1) ^ 1, guard)) break;
-      mbar_arrive_expect_tx(bar(B_QFULL), 128 * 64);
-      tma_load_2d(sb + OFF_QR, &tm_qr, bar(B_QFULL), xr, (b * p.s_q + i) * 128, pol_q);
-      q_last = qn;
+      if (lane == 0) {
+        if (!wait(bar(C::B_QEMPTY), (qn & 1) ^ 1, guard)) stop = true;
+        else {
+          mbar_arrive_expect_tx(bar(C::B_QFULL), 128 * 64);
+          tma_load_2d(sb + C::OFF_QR, &tm_qr, bar(C::B_QFULL), xr, (b * p.s_q + i) * 128, pol_q);
+          q_last = qn;
+        }
+      }
+      if (kSparse && !warp_ok(!stop)) stop = true;
+      if (stop) break;
       ++qn;
-      for (int t = pc.t0; t < pc.t0 + kNS && t < pc.t1; ++t) prefetch_tile(page_of(b, t));
+      if constexpr (!kSparse)
+        for (int t = pc.t0; t < pc.t0 + NS && t < pc.t1; ++t) prefetch_tile(page_of(b, t));
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const int s = g % kNS;
-        const int page = page_of(b, t);
-        if (t + kPrefetch < pc.t1) prefetch_tile(page_of(b, t + kPrefetch));
-        if (!wait(bar(B_EMPTY + s), ((g / kNS) & 1) ^ 1, guard)) { stop = true; break; }
-        const uint32_t slot = sb + OFF_RING + s * kSlot;
-        mbar_arrive_expect_tx(bar(B_FULL + s), kSlot);
+        const int s = g % NS;
+        if constexpr (!kSparse) {
+          const int page = page_of(b, t);
+          if (t + C::kPrefetch < pc.t1) prefetch_tile(page_of(b, t + C::kPrefetch));
+          if constexpr (kFp8) {
+            // raw e4m3 + scales into the staging ring, converted by the dequant warps
+            const int rs = g % kRawNS;
+            if (!wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
+            const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), kRawLat + kRawSc);
+            tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), 256 * (int)rank, page * kTile, pol_kv);
+            tma_load_2d(raw + kRawLat, &tm_sc, bar(C::B_RFULL + rs), 512, page * kTile, pol_kv);
+            last_rg[rs] = g;
+          }
+          if (!wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard)) { stop = true; break; }
+          const uint32_t slot = sb + C::OFF_RING + s * kSlot;
+          if constexpr (kFp8) {
+            // the RoPE dims are bf16 in the row: straight into the operand slot
+            mbar_arrive_expect_tx(bar(C::B_FULL + s), kRChunk);
+            tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), 528 + 64 * (int)rank, page * kTile, pol_kv);
+          } else {
+            mbar_arrive_expect_tx(bar(C::B_FULL + s), kSlot);
 #pragma unroll
-        for (int ci = 0; ci < 4; ++ci)
-          tma_load_2d(slot + ci * kKChunk, &tm_kv, bar(B_FULL + s), 256 * (int)rank + 64 * ci, page * kTile, pol_kv);
-        tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(B_FULL + s), xr, page * kTile, pol_kv);
-        last_g[s] = g;
+            for (int ci = 0; ci < 4; ++ci)
+              tma_load_2d(slot + ci * kKChunk, &tm_kv, bar(C::B_FULL + s), 256 * (int)rank + 64 * ci, page * kTile,
+                          pol_kv);
+            tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), xr, page * kTile, pol_kv);
+          }
+          last_g[s] = g;
+        } else {
+          // sparse: one bulk copy per valid row and field, issued by the whole warp
+          const int rs = g % kRawNS;
+          if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
+          const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+          const int32_t* irow = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
+          int idx[2];
+          bool okr[2];
+          int nvalid = 0;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int k = 64 * t + 32 * hh + lane;
+            idx[hh] = k < p.topk ? __ldg(irow + k) : -1;
+            okr[hh] = idx[hh] >= 0 && (int64_t)idx[hh] < p.num_rows;
+            nvalid += __popc(__ballot_sync(0xffffffffu, okr[hh]));
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), (uint32_t)nvalid * (256 + 16 + 64));
+          __syncwarp();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!okr[hh]) continue;
+            const int k = 32 * hh + lane;
+            const uint8_t* src = p.kv_fp8 + (int64_t)idx[hh] * kRowBytesFp8;
+            bulk_load(raw + k * 256, src + 256 * rank, 256, bar(C::B_RFULL + rs), pol_kv);
+            bulk_load(raw + kRawLat + k * 16, src + 512, 16, bar(C::B_RFULL + rs), pol_kv);
+            bulk_load(raw + kRawLat + kRawSc + k * 64, src + 528 + 64 * rank, 64, bar(C::B_RFULL + rs), pol_kv);
+          }
+          last_rg[rs] = g;
+          // the operand slot is filled by the dequant warps; this arrive only
+          // completes the producer's share of the barrier
+          if (!warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) { stop = true; break; }
+          if (lane == 0) mbar_arrive(bar(C::B_FULL + s));
+          last_g[s] = g;
+        }
       }
     }
     // never leave with a copy in flight into this CTA's shared memory
-    for (int s = 0; s < kNS; ++s)
-      if (last_g[s] >= 0) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s)
+        if (last_g[s] >= 0) {
+          const uint64_t t_0 = globaltimer();
+          while (!mbar_try_wait(bar(C::B_FULL + s), (last_g[s] / NS) & 1) && globaltimer() - t_0 < 200000000ull) {}
+        }
+      for (int s = 0; s < kRawNS; ++s)
+        if (last_rg[s] >= 0) {
+          const uint64_t t_0 = globaltimer();
+          while (!mbar_try_wait(bar(C::B_RFULL + s), (last_rg[s] / kRawNS) & 1) && globaltimer() - t_0 < 200000000ull) {}
+        }
+      if (q_last >= 0) {
         const uint64_t t_0 = globaltimer();
-        while (!mbar_try_wait(bar(B_FULL + s), (last_g[s] / kNS) & 1) && globaltimer() - t_0 < 200000000ull) {}
+        while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && globaltimer() - t_0 < 200000000ull) {}
       }
-    if (q_last >= 0) {
-      const uint64_t t_0 = globaltimer();
-      while (!mbar_try_wait(bar(B_QFULL), q_last & 1) && globaltimer() - t_0 < 200000000ull) {}
+    }
+  } else if (kFp8 && ok && (warp == 2 || warp == 3)) {
+    // ---------------- dequant: e4m3 x fp32 scale -> fp16 operand tiles ----------------
+    // (fp16 keeps 11 bits of the product; the latent QK^T and P.V of FP8
+    // caches run as fp16 x fp16, the RoPE QK^T stays bf16 x bf16)
+    const int tid = threadIdx.x - 64;  // 0..63
+    PieceIter it(p, part);
+    Piece pc;
+    int g = 0;
+    bool failed = false;
+    while (!failed && it.next(pc)) {
+      for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+        const int rs = g % kRawNS, s = g % NS;
+        const uint64_t vmask = tile_mask<kSparse>(p, pc.v, t, pc.len, false);
+        if (!warp_ok(wait(bar(C::B_RFULL + rs), (g / kRawNS) & 1, guard)) ||
+            !warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) {
+          failed = true;
+          break;
+        }
+        const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+        const uint32_t slot = sb + C::OFF_RING + s * kSlot;
+        const float* scales = reinterpret_cast<const float*>(smem + C::OFF_RAW + rs * kRawSlot + kRawLat);
+        // 64 rows x 32 units of 8 values; consecutive lanes take consecutive
+        // units of one row (conflict-free 8-B loads, 16-B swizzled stores)
+#pragma unroll 4
+        for (int it2 = 0; it2 < 32; ++it2) {
+          const int id = it2 * 64 + tid;
+          const int row = id >> 5, unit = id & 31;
+          uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+          if ((vmask >> row) & 1ull) {
+            uint32_t lo, hi;
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 256 + unit * 8));
+            const float sc = scales[row * 4 + 2 * rank + (unit >> 4)];
+            const float2 a = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)));
+            const float2 b2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)));
+            const float2 c2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)));
+            const float2 d2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)));
+            w0 = pack_f16x2_sat(a.x * sc, a.y * sc);
+            w1 = pack_f16x2_sat(b2.x * sc, b2.y * sc);
+            w2 = pack_f16x2_sat(c2.x * sc, c2.y * sc);
+            w3 = pack_f16x2_sat(d2.x * sc, d2.y * sc);
+          }
+          st_shared_v4(slot + (unit >> 3) * kKChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
+        }
+        if constexpr (kSparse) {
+          // RoPE: staged rows -> 64-byte-swizzled operand chunk
+#pragma unroll
+          for (int it2 = 0; it2 < 4; ++it2) {
+            const int id = it2 * 64 + tid;
+            const int row = id >> 2, u = id & 3;
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if ((vmask >> row) & 1ull) v4 = ld_shared_v4f(raw + kRawLat + kRawSc + row * 64 + u * 16);
+            st_shared_v4(slot + 4 * kKChunk + row * 64 + ((u ^ ((row >> 1) & 3)) << 4), __float_as_uint(v4.x),
+                         __float_as_uint(v4.y), __float_as_uint(v4.z), __float_as_uint(v4.w));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(C::B_FULL + s));
+          mbar_arrive(bar(C::B_REMPTY + rs));
+        }
+      }
     }
   } else if (ok && warp == 1 && lane == 0) {
     // ---------------- UMMA issuer: issues whichever of QK^T / P.V is ready ----------------
-    constexpr uint32_t idesc_qk = idesc_f16(128, 64, !kFp16, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(128, 256, !kFp16, false, true);
+    // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
+    // caches) and of the RoPE QK^T (the cache's RoPE dims: bf16 unless fp16)
+    constexpr bool kLatBf16 = !(kFp16 || kFp8);
+    constexpr uint32_t idesc_qk = idesc_f16(128, 64, kLatBf16, false, false);
+    constexpr uint32_t idesc_qr = idesc_f16(128, 64, !kFp16, false, false);
+    constexpr uint32_t idesc_pv = idesc_f16(128, 256, kLatBf16, false, true);
     // descriptors: +2 in the low word advances the start address by 32 B (16
     // elements of K), +128 by 2048 B (16 tokens of the MN-major V operand)
-    const uint64_t d_p = sdesc_sw128(sb + OFF_P, 16, 1024);
-    const uint64_t d_qr = sdesc_sw64(sb + OFF_QR, 16, 512);
+    const uint64_t d_p = sdesc_sw128(sb + C::OFF_P, 16, 1024);
+    const uint64_t d_qr = sdesc_sw64(sb + C::OFF_QR, 16, 512);
     PieceIter it(p, part);
     Piece pc;
     bool have = it.next(pc);
@@ -275,17 +477,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t first_bits = 0;       // bit (g & 31): tile g is the first of its piece
     int piece_of[4] = {0, 0, 0, 0};
     uint64_t t_last = globaltimer();
-    bool failed = false;
     while (true) {
       bool progressed = false;
       if (have) {
-        if (!q_ready && mbar_test(bar(B_QFULL), k_piece & 1)) q_ready = true;
-        const int s = qk_g % kNS, sbuf = qk_g & 1;
-        if (q_ready && mbar_test(bar(B_FULL + s), (qk_g / kNS) & 1) &&
-            mbar_test(bar(B_SEMPTY + sbuf), ((qk_g >> 1) & 1) ^ 1)) {
+        if (!q_ready && mbar_test(bar(C::B_QFULL), k_piece & 1)) q_ready = true;
+        const int s = qk_g % NS, sbuf = qk_g & 1;
+        if (q_ready && mbar_test(bar(C::B_FULL + s), (qk_g / NS) & 1) &&
+            mbar_test(bar(C::B_SEMPTY + sbuf), ((qk_g >> 1) & 1) ^ 1)) {
           tc_fence_after();
           const uint32_t dS = tmem + kColS + 64u * sbuf;
-          const uint32_t slot = sb + OFF_RING + s * kSlot;
+          const uint32_t slot = sb + C::OFF_RING + s * kSlot;
           const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
           const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
 #pragma unroll
@@ -295,15 +496,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               umma_ts(dS, tmem + kColQ + 32u * ci + 8u * k, d_k + (uint64_t)(ci * (kKChunk >> 4) + 2 * k), idesc_qk,
                       (ci | k) ? 1u : 0u);
           }
-          umma_ss(dS, d_qr, d_kr, idesc_qk, 1u);
-          umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qk, 1u);
-          umma_commit(bar(B_SFULL + sbuf));
+          umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
+          umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
+          umma_commit(bar(C::B_SFULL + sbuf));
           const bool first = qk_t == pc.t0;
           first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
           piece_of[qk_g & 3] = k_piece;
           ++qk_g;
           if (++qk_t == pc.t1) {
-            umma_commit(bar(B_QEMPTY));
+            umma_commit(bar(C::B_QEMPTY));
             have = it.next(pc);
             if (have) qk_t = pc.t0;
             ++k_piece;
@@ -312,18 +513,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           progressed = true;
         }
       }
-      if (pv_g < qk_g && mbar_test(bar(B_PFULL), pv_g & 1)) {
+      if (pv_g < qk_g && mbar_test(bar(C::B_PFULL), pv_g & 1)) {
         const bool first = (first_bits >> (pv_g & 31)) & 1u;
         const int pk = piece_of[pv_g & 3];
-        if (!first || pk == 0 || mbar_test(bar(B_OEMPTY), (pk - 1) & 1)) {
+        if (!first || pk == 0 || mbar_test(bar(C::B_OEMPTY), (pk - 1) & 1)) {
           tc_fence_after();
-          const uint64_t d_v = sdesc_sw128(sb + OFF_RING + (pv_g % kNS) * kSlot, kKChunk, 1024);
+          const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (pv_g % NS) * kSlot, kKChunk, 1024);
           umma_ss(tmem, d_p, d_v, idesc_pv, first ? 0u : 1u);
           umma_ss(tmem, d_p + 2, d_v + 128, idesc_pv, 1u);
           umma_ss(tmem, d_p + 4, d_v + 256, idesc_pv, 1u);
           umma_ss(tmem, d_p + 6, d_v + 384, idesc_pv, 1u);
-          umma_commit(bar(B_PEMPTY));
-          umma_commit(bar(B_EMPTY + pv_g % kNS));
+          umma_commit(bar(C::B_PEMPTY));
+          umma_commit(bar(C::B_EMPTY + pv_g % NS));
           ++pv_g;
           progressed = true;
         }
@@ -332,20 +533,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (progressed) {
         t_last = globaltimer();
       } else {
-        if (*abort_flag) { failed = true; break; }
+        if (*abort_flag) break;
         if (globaltimer() - t_last > guard.limit_ns) {
           *abort_flag = 1u;
           atomicOr(p.status, STATUS_TIMEOUT);
-          failed = true;
           break;
         }
       }
     }
-    (void)failed;
     // every UMMA issued above has completed before TMEM is released
-    umma_commit(bar(B_DRAIN));
+    umma_commit(bar(C::B_DRAIN));
     const uint64_t t_0 = globaltimer();
-    while (!mbar_try_wait(bar(B_DRAIN), 0) && globaltimer() - t_0 < 200000000ull) {}
+    while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t_0 < 200000000ull) {}
   } else if (ok && warp >= 4) {
     // ---------------- softmax / exchange / epilogue ----------------
     const int q4 = warp & 3;                              // TMEM lane quadrant
@@ -353,23 +552,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int h = 32 * q4 + lane;                         // head = TMEM lane
     const int sid = threadIdx.x - 128;                    // 0..255 among softmax threads
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xr_row = sb + OFF_XR + h * 128;        // same offsets in both CTAs
-    const uint32_t xs_row = sb + OFF_XS + h * 128;
-    const uint32_t xr_remote = mapa(sb + OFF_XR, peer);
-    const uint32_t xfull_remote = mapa(bar(B_XFULL), peer);
-    const uint32_t xempty_remote = mapa(bar(B_XEMPTY), peer);
-    const uint32_t p_row = sb + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
-    float* mx = reinterpret_cast<float*>(smem + OFF_MX);  // [tile parity][half][row]
-    float* lx = mx + 2 * 256;                             // [half][row]
-    const float* xr_m = reinterpret_cast<const float*>(smem + OFF_XR + kXE);
-    float* xs_m = reinterpret_cast<float*>(smem + OFF_XS + kXE);
+    const uint32_t xr_row = sb + C::OFF_XR + h * 128;     // same offsets in both CTAs
+    const uint32_t xs_row = sb + C::OFF_XS + h * 128;
+    const uint32_t xr_remote = mapa(sb + C::OFF_XR, peer);
+    const uint32_t xfull_remote = mapa(bar(C::B_XFULL), peer);
+    const uint32_t xempty_remote = mapa(bar(C::B_XEMPTY), peer);
+    const uint32_t p_row = sb + C::OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
+    float* mx = reinterpret_cast<float*>(smem + C::OFF_MX);  // [tile parity][half][row]
+    float* lx = mx + 2 * 256;                                // [half][row]
+    const float* xr_m = reinterpret_cast<const float*>(smem + C::OFF_XR + kXE);
+    float* xs_m = reinterpret_cast<float*>(smem + C::OFF_XS + kXE);
     const float sl2 = p.scale_log2;
     const uint32_t pair_bar = kPairBar + q4;
 
     // copy this CTA's 256 latent dims of every head's query row into TMEM
     // (each of the two warps of a quadrant copies 128 of them)
     auto load_q = [&](const Piece& q_pc, int q_idx) -> bool {
-      if (q_idx > 0 && !warp_ok(wait(bar(B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
+      if (q_idx > 0 && !warp_ok(wait(bar(C::B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
       const int b = q_pc.v % p.batch, i = q_pc.v / p.batch;
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const uint16_t*>(p.q) + ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank + 128 * c);
@@ -379,36 +578,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint4 x = __ldg(src + k);
         r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
       }
+      if constexpr (kFp8) {  // latent operands of FP8 caches are fp16
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          r[k] = pack_f16x2_sat(__uint_as_float(r[k] << 16), __uint_as_float(r[k] & 0xFFFF0000u));
+      }
       tc_fence_after();
       tmem_st32(tl + kColQ + 64u * c, r);
       tmem_st32(tl + kColQ + 64u * c + 32u, r + 32);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_QFULL));
+      if (lane == 0) mbar_arrive(bar(C::B_QFULL));
       return true;
     };
     // Tile gg: read this warp's 32 partial-score columns from TMEM, E_r =
     // exp2(x - m_r) with x = S_r * scale * log2e and m_r the partial row max
-    // over the nvg valid tokens (masked tokens get E = 0), kept as fp16 pairs
-    // in `e`; stage E_r and m_r and copy them to the peer.
-    auto send_partial = [&](int gg, int nvg, uint32_t* e, float& m_own) -> bool {
+    // over the valid tokens (vmask; masked tokens get E = 0), kept as fp16
+    // pairs in `e`; stage E_r and m_r and copy them to the peer.
+    auto send_partial = [&](int gg, uint32_t vm, uint32_t* e, float& m_own) -> bool {
       const int sbuf = gg & 1;
-      if (!warp_ok(wait(bar(B_SFULL + sbuf), (gg >> 1) & 1, guard))) return false;
+      if (!warp_ok(wait(bar(C::B_SFULL + sbuf), (gg >> 1) & 1, guard))) return false;
       tc_fence_after();
       uint32_t sr[32];
       tmem_ld32(tl + kColS + 64u * sbuf + 32u * c, sr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SEMPTY + sbuf));
-      const int nvc = nvg - 32 * c;  // valid columns in this half
+      if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + sbuf));
       float x[32];
       float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
-        x[k] = k < nvc ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
-        x[k + 1] = k + 1 < nvc ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
+        x[k] = (vm >> k) & 1u ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
+        x[k + 1] = (vm >> (k + 1)) & 1u ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
         m0 = fmaxf(m0, x[k]);
         m1 = fmaxf(m1, x[k + 1]);
       }
@@ -421,14 +624,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 16; ++u) e[u] = pack_f16x2(exp2_approx(x[2 * u] - mref), exp2_approx(x[2 * u + 1] - mref));
       // the peer has consumed the previous message: staging and its receive
       // buffer are free
-      if (!warp_ok(wait_cluster(bar(B_XEMPTY), (gg & 1) ^ 1, guard))) return false;
+      if (!warp_ok(wait_cluster(bar(C::B_XEMPTY), (gg & 1) ^ 1, guard))) return false;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         st_shared_v4(xs_row + (((4 * c + u) ^ (h & 7)) << 4), e[4 * u], e[4 * u + 1], e[4 * u + 2], e[4 * u + 3]);
       if (c == 0) xs_m[h] = m_own;
       fence_proxy_async_smem();
       named_sync(kSoftmaxBar, 256);
-      if (sid == 0) bulk_copy_to_peer(xr_remote, sb + OFF_XS, kXBytes, xfull_remote);
+      if (sid == 0) bulk_copy_to_peer(xr_remote, sb + C::OFF_XS, kXBytes, xfull_remote);
       return true;
     };
 
@@ -443,14 +646,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     while (have && !failed) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       float m = -INFINITY, l_half = 0.f;
-      int nv_cur = dense_valid(p, b, pc.t0, pc.len, false);
-      if (!send_partial(g, nv_cur, cur, m_cur)) { failed = true; break; }
+      uint64_t vm_cur = tile_mask<kSparse>(p, pc.v, pc.t0, pc.len, rank == 0 && sid < 32);
+      if (!send_partial(g, (uint32_t)(vm_cur >> (32 * c)), cur, m_cur)) { failed = true; break; }
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const int nv = nv_cur;
-        if (nv == 0 && sid == 0 && rank == 0) atomicOr(p.status, STATUS_INDEX);  // unreachable page
+        const uint64_t vm = vm_cur;
         // (1) receive the peer's E and m of tile g
-        if (sid == 0) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
-        if (!warp_ok(wait_cluster(bar(B_XFULL), g & 1, guard))) { failed = true; break; }
+        if (sid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
+        if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
         uint32_t ep[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -469,8 +671,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float m_mine = m_cur;
         // (2) exponentiate and send tile g+1 (same piece)
         if (t + 1 < pc.t1) {
-          nv_cur = dense_valid(p, b, t + 1, pc.len, false);
-          if (!send_partial(g + 1, nv_cur, cur, m_cur)) { failed = true; break; }
+          vm_cur = tile_mask<kSparse>(p, pc.v, t + 1, pc.len, rank == 0 && sid < 32);
+          if (!send_partial(g + 1, (uint32_t)(vm_cur >> (32 * c)), cur, m_cur)) { failed = true; break; }
         }
         // (3) P of tile g: E_0 * E_1 * 2^(m_0 + m_1 - m_ref), lazy rescale
         // against the running reference max (P stays <= 256)
@@ -489,12 +691,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float a1 = fo.y * fq.y * cf;
           rs0 += a0;
           rs1 += a1;
-          pw[u] = kFp16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+          pw[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
         }
         l_half = l_half * alpha + (rs0 + rs1);
         m = m_use;
         // the previous P . V has finished: P buffer and O are free
-        if (g > 0 && !warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
+        if (g > 0 && !warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, resc) && t != pc.t0) {
 #pragma unroll 1
@@ -509,15 +711,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        if (nv < kTile) {
+        if (!kFp8 && vm != ~0ull) {
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
-          // turn into NaN inside P . V
-          const uint32_t slot = sb + OFF_RING + (g % kNS) * kSlot;
-          const int nz = kTile - (nv > 0 ? nv : 0);
-          const int nrow = nz * 4;  // rows x 4 V chunks
-          for (int e2 = sid; e2 < nrow * 8; e2 += 256) {
-            const int rr = e2 >> 3, ch = rr / nz, row = kTile - nz + rr % nz;
-            st_shared_v4(slot + ch * kKChunk + row * 128 + (e2 & 7) * 16, 0u, 0u, 0u, 0u);
+          // turn into NaN inside P . V (the dequant warps do this for FP8 rows)
+          const uint32_t slot = sb + C::OFF_RING + (g % NS) * kSlot;
+          for (int e2 = sid; e2 < 64 * 32; e2 += 256) {
+            const int row = e2 >> 5, u = e2 & 31;
+            if (!((vm >> row) & 1ull))
+              st_shared_v4(slot + (u >> 3) * kKChunk + row * 128 + (u & 7) * 16, 0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
@@ -526,7 +727,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL));
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL));
       }
       if (failed) break;
       // the next piece's Q goes into TMEM before this piece's epilogue, so
@@ -537,7 +738,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       lx[c * 128 + h] = l_half;
       named_sync(pair_bar, 64);
       const float l = lx[h] + lx[128 + h];
-      if (!warp_ok(wait(bar(B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
+      if (!warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -575,7 +776,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OEMPTY));
+      if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
       pc = nx;
       have = have_next;
     }

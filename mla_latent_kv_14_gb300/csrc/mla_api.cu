@@ -72,16 +72,23 @@ cudaError_t set_smem(K kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+template <int kMode>
+cudaError_t set_mode_smem() {
+  return set_smem(dense::mla_decode_kernel<kMode>, dense::Cfg<kMode>::kSmemBytes);
+}
+
 cudaError_t prepare_device(int dev) {
   cudaError_t err = cudaSuccess;
   std::call_once(g_attr_once[dev], [&] {
-    err = set_smem(dense::mla_decode_dense_kernel<false>, dense::kSmemBytes);
-    if (err == cudaSuccess) err = set_smem(dense::mla_decode_dense_kernel<true>, dense::kSmemBytes);
+    err = set_mode_smem<dense::MODE_BF16>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP16>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8_SPARSE>();
     if (err == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2, 1, 1);
       cfg.blockDim = dim3(dense::kThreads, 1, 1);
-      cfg.dynamicSmemBytes = dense::kSmemBytes;
+      cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_BF16>::kSmemBytes;
       cudaLaunchAttribute at[1];
       at[0].id = cudaLaunchAttributeClusterDimension;
       at[0].val.clusterDim.x = 2;
@@ -90,10 +97,11 @@ cudaError_t prepare_device(int dev) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      err = cudaOccupancyMaxActiveClusters(&n, dense::mla_decode_dense_kernel<false>, &cfg);
+      err = cudaOccupancyMaxActiveClusters(&n, dense::mla_decode_kernel<dense::MODE_BF16>, &cfg);
       if (err == cudaSuccess) g_parts[dev].store(n > 0 ? n : 1);
     }
   });
+  if (err == cudaSuccess && g_parts[dev].load() <= 0) err = cudaErrorInitializationError;
   return err;
 }
 
@@ -181,7 +189,8 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   if (workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
   if (num_blocks * (int64_t)page_block >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
   if (h_q != 128) return MLA_ERR_UNSUPPORTED;
-  if (is_fp8 || indices) return MLA_ERR_UNSUPPORTED;
+  if (indices && !is_fp8) return MLA_ERR_UNSUPPORTED;                 // token-sparse decode reads FP8 rows
+  if (is_fp8 && q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED; // FP8 rows pair with bf16 queries
   const int64_t qrows = (int64_t)batch * s_q * h_q;
   if (qrows >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
 
@@ -191,15 +200,30 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   MLA_CUDA(prepare_device(dev));
 
   const bool fp16 = q_dtype == MLA_DTYPE_FP16;
+  const int mode = is_fp8 ? (indices ? dense::MODE_FP8_SPARSE : dense::MODE_FP8)
+                          : (fp16 ? dense::MODE_FP16 : dense::MODE_BF16);
   const CUtensorMapDataType dt = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // Q: the 32-dim RoPE halves (64-B swizzle); KV: 64-dim latent chunks
-  // (128-B swizzle) and 32-dim RoPE halves (64-B swizzle)
-  CUtensorMap tm_qr, tm_kv, tm_kvr;
   const uint64_t kvrows = (uint64_t)(num_blocks * page_block);
-  if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&tm_kv, kvcache, dt, 2, kvrows, kDK, kDK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tm_kvr, kvcache, dt, 2, kvrows, kDK, kDK * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+  // Q: the 32-dim RoPE halves (64-B swizzle). KV, 16-bit caches: 64-dim latent
+  // chunks (128-B swizzle) and 32-dim RoPE halves (64-B swizzle). KV, FP8 rows
+  // (bytes): 256 e4m3 per CTA, the 16 scale bytes, 64 RoPE bytes (64-B swizzle).
+  CUtensorMap tm_qr, tm_kv, tm_kvr, tm_sc;
+  if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
+  if (mode == dense::MODE_FP8_SPARSE) {
+    tm_kv = tm_kvr = tm_sc = tm_qr;  // rows are fetched by address
+  } else if (mode == dense::MODE_FP8) {
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map(&tm_kv, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sc, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MLA_ERR_CUDA;
+  } else {
+    if (!make_map(&tm_kv, kvcache, dt, 2, kvrows, kDK, kDK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_kvr, kvcache, dt, 2, kvrows, kDK, kDK * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MLA_ERR_CUDA;
+    tm_sc = tm_kv;
+  }
 
   const int64_t S = max_splits(batch * s_q, parts);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -208,7 +232,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.block_table = block_table;
   p.seqlens = cache_seqlens;
   p.indices = indices;
-  p.kv_fp8 = nullptr;
+  p.kv_fp8 = static_cast<const uint8_t*>(kvcache);
   p.meta = static_cast<const int32_t*>(metadata);
   p.split_off = num_splits;
   p.out = out;
@@ -233,12 +257,26 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * parts, 1, 1);
     cfg.blockDim = dim3(dense::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = dense::kSmemBytes;
     cfg.stream = st;
-    if (fp16)
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<true>, tm_qr, tm_kv, tm_kvr, p));
-    else
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_dense_kernel<false>, tm_qr, tm_kv, tm_kvr, p));
+    switch (mode) {
+      case dense::MODE_BF16:
+        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_BF16>::kSmemBytes;
+        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_BF16>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
+        break;
+      case dense::MODE_FP16:
+        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP16>::kSmemBytes;
+        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP16>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
+        break;
+      case dense::MODE_FP8:
+        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP8>::kSmemBytes;
+        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP8>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
+        break;
+      default:
+        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP8_SPARSE>::kSmemBytes;
+        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP8_SPARSE>, tm_qr, tm_kv, tm_kvr,
+                                    tm_sc, p));
+        break;
+    }
   }
   if (!(stages & STAGE_COMBINE)) return MLA_OK;
 

@@ -243,3 +243,90 @@ def test_schedule_covers_every_tile_once():
         for v in range(B * s_q):
             assert (seen[v] == 1).all(), (parts, v)
             assert off[v + 1] - off[v] == npieces[v]
+
+
+# ---------------------------------------------------------------------------
+# FP8 656-byte cache: dense paged and token-sparse
+# ---------------------------------------------------------------------------
+def _fp8_oracle_rows(rows_bf16):
+    """Oracle view of an FP8 cache: quantise (oracle) then dequantise in float64."""
+    raw = oracle.quantize_kv_fp8(rows_bf16)
+    return raw, oracle.dequantize_kv_fp8(raw)
+
+
+@pytest.mark.parametrize("lens,s_q,causal", [([256, 193], 1, False), ([65, 1, 700], 1, False),
+                                             ([300, 64], 2, True)])
+def test_fp8_dense_paged(lens, s_q, causal):
+    case = synth.make_dense_case(lens, s_q=s_q, causal=causal, seed=20 + len(lens), outlier_channels=4)
+    dev = "cuda"
+    raw = mla.mla_quantize_kv_fp8(case.kv_rows.to(dev))
+    raw_ref, deq = _fp8_oracle_rows(case.kv_rows)
+    assert (raw.cpu().numpy() == raw_ref).all()
+    kv8 = raw.view(case.num_blocks, 64, 1, 656)
+    sl = case.cache_seqlens.to(dev)
+    meta, ns = mla.mla_get_metadata(sl, s_q, 128, causal=causal, is_fp8=True)
+    _status_clear()
+    out, lse = mla.mla_decode_with_kvcache(case.q.to(dev), kv8, case.block_table.to(dev), sl, 512, meta, ns,
+                                           softmax_scale=case.softmax_scale, causal=causal, is_fp8=True)
+    torch.cuda.synchronize()
+    assert _status_clear()[0] == 0
+    ro, rl, _ = oracle.mla_decode(oracle.to_f64(case.q), deq, cache_seqlens=case.cache_seqlens.numpy(),
+                                  block_table=case.block_table.numpy(), softmax_scale=case.softmax_scale, causal=causal)
+    assert_close_attn(out, lse, ro, rl, f"fp8 dense {lens}")
+
+
+def _run_sparse(case, raw_dev, dev="cuda", parts=None):
+    B = case.batch
+    kv8 = raw_dev.view(-1, 64, 1, 656)
+    idx = case.indices.to(dev)
+    meta, ns = mla.mla_get_metadata(None, case.s_q, 128, batch=B, topk=idx.shape[-1], is_fp8=True, device=dev,
+                                    num_sm_parts=parts)
+    out, lse = mla.mla_decode_with_kvcache(case.q.to(dev), kv8, None, None, 512, meta, ns,
+                                           softmax_scale=case.softmax_scale, is_fp8=True, indices=idx)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("s_q,topk,parts", [(1, 256, None), (2, 100, None), (1, 200, 3), (2, 64, 1)])
+def test_fp8_sparse(s_q, topk, parts):
+    case = synth.make_sparse_case(2, s_q, topk, tokens_per_request=2048, seed=30 + topk, outlier_channels=4)
+    dev = "cuda"
+    raw = mla.mla_quantize_kv_fp8(case.kv_rows.to(dev))
+    raw_ref, deq = _fp8_oracle_rows(case.kv_rows)
+    assert (raw.cpu().numpy() == raw_ref).all()
+    _status_clear()
+    out, lse = _run_sparse(case, raw, parts=parts)
+    assert _status_clear()[0] == 0
+    ro, rl, bad = oracle.mla_decode(oracle.to_f64(case.q), deq, indices=case.indices.numpy(),
+                                    softmax_scale=case.softmax_scale)
+    assert not bad
+    assert_close_attn(out, lse, ro, rl, f"fp8 sparse s_q={s_q} topk={topk}")
+
+
+def test_fp8_sparse_out_of_range_index_reported_and_skipped():
+    case = synth.make_sparse_case(1, 1, 128, tokens_per_request=1024, seed=41)
+    idx = case.indices.clone()
+    idx[0, 0, 3] = 1 << 30          # beyond the cache
+    idx[0, 0, 70] = -5              # negative, not the -1 padding
+    case.indices = idx
+    dev = "cuda"
+    raw = mla.mla_quantize_kv_fp8(case.kv_rows.to(dev))
+    _, deq = _fp8_oracle_rows(case.kv_rows)
+    _status_clear()
+    out, lse = _run_sparse(case, raw)
+    st, bits = _status_clear()
+    assert st == 4 and bits & 1
+    ro, rl, bad = oracle.mla_decode(oracle.to_f64(case.q), deq, indices=idx.numpy(),
+                                    softmax_scale=case.softmax_scale)
+    assert bad
+    assert_close_attn(out, lse, ro, rl, "fp8 sparse bad index")
+
+
+def test_fp8_sparse_all_invalid_query():
+    case = synth.make_sparse_case(2, 1, 64, tokens_per_request=512, seed=42)
+    idx = case.indices.clone()
+    idx[1] = -1
+    case.indices = idx
+    raw = mla.mla_quantize_kv_fp8(case.kv_rows.to("cuda"))
+    out, lse = _run_sparse(case, raw)
+    assert (out[1].float().cpu() == 0).all() and torch.isneginf(lse[1].cpu()).all()
