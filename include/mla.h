@@ -162,6 +162,39 @@ MLA_API mla_status mla_combine_splits(const void* q, int q_dtype, const void* kv
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_with_kvcache without a caller-supplied workspace, for callers that
+ * cannot allocate device memory on demand (cudaMalloc may synchronise the
+ * device and can fail once memory is committed -- unacceptable inside a
+ * fixed-latency serving loop, or for a plug-in whose host application owns
+ * every device allocation). The pages describe no such entry point; it is an
+ * engineering addition of this library.
+ *
+ * Same arguments and results as mla_decode_with_kvcache, except:
+ *  - the split-KV scratch is a fixed 32 MiB array inside the library, one per
+ *    device, held until the process exits; a shape whose mla_workspace_size()
+ *    exceeds 32 MiB is rejected with MLA_ERR_INVALID_ARG (use
+ *    mla_decode_with_kvcache for it);
+ *  - nothing is allocated or freed;
+ *  - all calls on a device share the array: calls that may overlap on the GPU
+ *    (e.g. on different streams) race and must be serialised by the caller;
+ *  - the first call on a device looks up the array's device address (once,
+ *    with that device current); make that first call before any stream
+ *    capture;
+ *  - status (device, optional, 4-B aligned): receives the device-side status
+ *    bits of this call (1 = index/page skipped, 2 = wait timeout, 4 = stale
+ *    metadata), or NULL to discard them.
+ */
+MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, const void* kvcache,
+                                                   int64_t num_blocks, int page_block,
+                                                   const int32_t* block_table, int max_blocks,
+                                                   const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                                                   int head_dim_v, const void* metadata,
+                                                   const int32_t* num_splits, int num_sm_parts,
+                                                   float softmax_scale, int causal, int is_fp8,
+                                                   const int32_t* indices, int topk, void* out, float* lse,
+                                                   uint32_t* status, void* stream);
+
+/*
  * Write the 656-byte FP8 cache rows ("FlashMLA 实战：MLA 注意力加速指南",
  * §FP8 缓存怎么把 KV 压掉四成): bytes [0,512) e4m3 codes of the 512 latent dims,
  * quantised per 128 values with scale = fp32(amax/448) (1.0 for an all-zero

@@ -61,6 +61,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.restype = c.c_int
             f.argtypes = lib.mla_decode_with_kvcache.argtypes
+        lib.mla_decode_with_kvcache_noalloc.restype = c.c_int
+        lib.mla_decode_with_kvcache_noalloc.argtypes = lib.mla_decode_with_kvcache.argtypes[:-3] + [vp, vp]
         lib.mla_quantize_kv_fp8.restype = c.c_int
         lib.mla_quantize_kv_fp8.argtypes = [vp, vp, c.c_int64, vp]
         lib.mla_read_status.restype = c.c_int
@@ -188,6 +190,40 @@ def mla_decode_splitkv(*args, **kw):
 def mla_combine_splits(*args, **kw):
     """Only the combine of :func:`mla_decode_with_kvcache` (after mla_decode_splitkv)."""
     return mla_decode_with_kvcache(*args, _entry="mla_combine_splits", **kw)
+
+
+def mla_decode_with_kvcache_noalloc(q: torch.Tensor, kvcache: torch.Tensor, block_table: Optional[torch.Tensor],
+                                    cache_seqlens: Optional[torch.Tensor], head_dim_v: int, metadata: Metadata,
+                                    num_splits: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+                                    causal: bool = False, is_fp8: bool = False,
+                                    indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                                    lse: Optional[torch.Tensor] = None,
+                                    status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Decode using the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory on demand). ``out``/``lse``
+    /``status`` are allocated here only when not given."""
+    lib = load_library()
+    B, s_q, h_q, d_k = q.shape
+    assert d_k == 576 and q.is_contiguous() and kvcache.is_contiguous()
+    dev = _dev(q.device)
+    num_blocks, page_block = int(kvcache.shape[0]), int(kvcache.shape[1])
+    if softmax_scale is None:
+        softmax_scale = d_k ** -0.5
+    if num_splits is None:
+        num_splits = metadata.num_splits
+    topk = int(indices.shape[-1]) if indices is not None else 0
+    if out is None:
+        out = torch.empty(B, s_q, h_q, head_dim_v, dtype=q.dtype, device=dev)
+    if lse is None:
+        lse = torch.empty(B, s_q, h_q, dtype=torch.float32, device=dev)
+    max_blocks = int(block_table.shape[1]) if block_table is not None else 0
+    st = lib.mla_decode_with_kvcache_noalloc(
+        _ptr(q), DTYPE_CODES[q.dtype], _ptr(kvcache), num_blocks, page_block, _ptr(block_table), max_blocks,
+        _ptr(cache_seqlens), B, s_q, h_q, head_dim_v, _ptr(metadata.meta), _ptr(num_splits), metadata.parts,
+        float(softmax_scale), int(causal), int(is_fp8), _ptr(indices), topk, _ptr(out), _ptr(lse), _ptr(status),
+        _stream(dev))
+    _check(st, "mla_decode_with_kvcache_noalloc")
+    return out, lse
 
 
 def mla_quantize_kv_fp8(kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:

@@ -348,3 +348,68 @@ mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of mla_decode_with_kvcache.
+//
+// Some callers cannot obtain device memory on demand: cudaMalloc may
+// synchronise the whole device and can fail once memory is committed, which a
+// serving loop with a fixed latency budget, or a plug-in running inside a host
+// application that owns every device allocation, cannot accept. For them the
+// split-KV scratch (the status word and the fp32 partial outputs of cut
+// requests) lives in one fixed device array compiled into this library. Every
+// GPU that loads the library holds its own copy of the array until the
+// process exits, and all calls on one device share that copy: calls that
+// overlap on the GPU (for example on two streams) race on it and must be
+// serialised by the caller.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kStaticWsBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+std::once_flag g_static_once[kMaxDevices];
+void* g_static_ptr[kMaxDevices];
+cudaError_t g_static_err[kMaxDevices];
+
+// Host code may not use g_static_ws directly (its name is a host-side stand-in,
+// not a device address): look the device address up once per device, with
+// that device current.
+void* static_ws_ptr(int dev, cudaError_t* err) {
+  std::call_once(g_static_once[dev], [&] {
+    void* ptr = nullptr;
+    g_static_err[dev] = cudaGetSymbolAddress(&ptr, g_static_ws);
+    g_static_ptr[dev] = g_static_err[dev] == cudaSuccess ? ptr : nullptr;
+    (void)cudaGetLastError();
+  });
+  *err = g_static_err[dev];
+  return g_static_ptr[dev];
+}
+}  // namespace
+
+extern "C" mla_status mla_decode_with_kvcache_noalloc(
+    const void* q, int q_dtype, const void* kvcache, int64_t num_blocks, int page_block, const int32_t* block_table,
+    int max_blocks, const int32_t* cache_seqlens, int batch, int s_q, int h_q, int head_dim_v, const void* metadata,
+    const int32_t* num_splits, int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+    void* out, float* lse, uint32_t* status, void* stream) {
+  const size_t need = mla_workspace_size(batch, s_q, h_q, parts);
+  if (need == 0) return MLA_ERR_INVALID_ARG;
+  if (need > kStaticWsBytes) return MLA_ERR_INVALID_ARG;  // beyond the fixed scratch: use mla_decode_with_kvcache
+  if (status && !aligned(status, 4)) return MLA_ERR_INVALID_ARG;
+  int dev = 0;
+  MLA_CUDA(cudaGetDevice(&dev));
+  if (dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  cudaError_t e = cudaSuccess;
+  void* ws = static_ws_ptr(dev, &e);
+  if (e != cudaSuccess || !ws) return MLA_ERR_CUDA;
+  // The array keeps the previous call's contents: the status word must start
+  // at zero (the fp32 partials are fully written before they are read).
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MLA_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st));
+  mla_status r = decode_impl(STAGE_SPLIT | STAGE_COMBINE, q, q_dtype, kvcache, num_blocks, page_block, block_table,
+                             max_blocks, cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
+                             softmax_scale, causal, is_fp8, indices, topk, out, lse, ws, kStaticWsBytes, stream);
+  // device-side problems (bad index or page, stale metadata, wait timeout) are
+  // recorded in the array's status word; copy them out for the caller
+  if (r == MLA_OK && status) MLA_CUDA(cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st));
+  return r;
+}
