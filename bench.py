@@ -31,13 +31,21 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode TFLOPS + KV GB/s (fraction of GB300 roofline), B=64 s_q=1 seqlen 8K"
 
 WORKLOADS = {
-    # name: (kind, params)
+    # dense BF16 paged cache (the headline is the first)
     "dense_bf16_b64_sq1_l8192": dict(kind="dense", batch=64, s_q=1, lens=("fixed", 8192), causal=False),
     "dense_bf16_b64_sq1_uniform": dict(kind="dense", batch=64, s_q=1, lens=("uniform", 4096, 12288), causal=False),
     "dense_bf16_b64_sq2_causal_l8192": dict(kind="dense", batch=64, s_q=2, lens=("fixed", 8192), causal=True),
     "dense_bf16_b64_sq2_causal_uniform": dict(kind="dense", batch=64, s_q=2, lens=("uniform", 4096, 12288),
                                               causal=True),
+    # 656-byte FP8 cache, paged, per-row outlier channels x8
+    "fp8_dense_b16_l32768": dict(kind="fp8", batch=16, s_q=1, lens=("fixed", 32768), causal=False),
+    # token-sparse over a 131072-token FP8 cache per request, 5% of the slots -1
+    "fp8_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False),
+    "fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False),
+    "fp8_sparse_b32_sq2_topk2048": dict(kind="sparse", batch=32, s_q=2, topk=2048, causal=False),
+    "fp8_sparse_b32_sq2_topk32768": dict(kind="sparse", batch=32, s_q=2, topk=32768, causal=False),
 }
+SPARSE_TOKENS = 131072
 DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"
 
 
@@ -53,24 +61,39 @@ def load_peaks():
 
 def workload_seqlens(w):
     import synth
+    if w["kind"] == "sparse":
+        return None
     if w["lens"][0] == "fixed":
         return [w["lens"][1]] * w["batch"]
     return [int(x) for x in synth.uniform_seqlens(w["batch"], w["lens"][1], w["lens"][2], seed=2)]
 
 
-def work_counts(seqlens, s_q, causal, h_q=128):
-    """Algorithmic FLOPs and bytes of one step (no partials, no expansion)."""
-    pairs = 0
-    for L in seqlens:
-        for i in range(s_q):
-            pairs += max(0, L - (s_q - 1 - i if causal else 0))
+def work_counts(seqlens, s_q, causal, h_q=128, row_bytes=1152, indices=None):
+    """Algorithmic FLOPs and bytes of one step (no partials, no expansion):
+    FLOPs = 2 * h_q * (576 + 512) per visible (query, key) pair; bytes = the
+    cache rows read once (1152 B bf16, 656 B fp8; a row shared by the query
+    positions of one request counts once) + q + out + lse + block table or
+    index list."""
+    if indices is not None:
+        import numpy as np
+        B = indices.shape[0]
+        valid = indices >= 0
+        pairs = int(valid.sum())
+        rows = sum(len(np.unique(indices[b][valid[b]])) for b in range(B))
+        kv = rows * row_bytes
+        meta = indices.size * 4
+    else:
+        B = len(seqlens)
+        pairs = 0
+        for L in seqlens:
+            for i in range(s_q):
+                pairs += max(0, L - (s_q - 1 - i if causal else 0))
+        kv = sum(seqlens) * row_bytes
+        meta = sum((L + 63) // 64 for L in seqlens) * 4 + B * 4
     flops = 2.0 * h_q * (576 + 512) * pairs
-    kv = sum(seqlens) * 576 * 2
-    B = len(seqlens)
     qb = B * s_q * h_q * 576 * 2
     ob = B * s_q * h_q * (512 * 2 + 4)
-    bt = sum((L + 63) // 64 for L in seqlens) * 4 + B * 4
-    return flops, kv + qb + ob + bt, kv
+    return flops, kv + qb + ob + meta, kv
 
 
 class ClockSampler:
@@ -126,8 +149,13 @@ class ClockSampler:
 
 def build_case(w, device):
     import synth
+    if w["kind"] == "sparse":
+        case = synth.make_sparse_case(w["batch"], w["s_q"], w["topk"], tokens_per_request=SPARSE_TOKENS, seed=0,
+                                      outlier_channels=4, device=device)
+        return case, None
     seqlens = workload_seqlens(w)
-    case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device)
+    case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device,
+                                 outlier_channels=4 if w["kind"] == "fp8" else 0)
     return case, seqlens
 
 
@@ -168,21 +196,37 @@ def run_ours(args, w, rank, world, device):
 
     torch.cuda.set_device(device)
     case, seqlens = build_case(w, device)
-    flops, algo_bytes, kv_bytes = work_counts(seqlens, w["s_q"], w["causal"])
-    q = case.q
-    kv = case.kvcache_paged()
-    bt = case.block_table.to(device)
-    sl = case.cache_seqlens.to(device)
+    kind = w["kind"]
     s_q, causal = w["s_q"], w["causal"]
+    is_fp8 = kind in ("fp8", "sparse")
+    q = case.q
+    bt = sl = idx = None
+    if kind == "sparse":
+        raw = mla.mla_quantize_kv_fp8(case.kv_rows)          # the FP8 cache, written by the library
+        case.kv_rows = None
+        kv = raw.view(-1, 64, 1, 656)
+        idx = case.indices.to(device)
+        flops, algo_bytes, kv_bytes = work_counts(None, s_q, False, row_bytes=656, indices=case.indices.numpy())
+        meta_args = dict(batch=q.shape[0], topk=idx.shape[-1], is_fp8=True, device=device)
+    else:
+        bt = case.block_table.to(device)
+        sl = case.cache_seqlens.to(device)
+        if kind == "fp8":
+            raw = mla.mla_quantize_kv_fp8(case.kv_rows)
+            kv = raw.view(case.num_blocks, 64, 1, 656)
+        else:
+            kv = case.kvcache_paged()
+        flops, algo_bytes, kv_bytes = work_counts(seqlens, s_q, causal, row_bytes=656 if is_fp8 else 1152)
+        meta_args = dict(causal=causal, is_fp8=is_fp8)
     out = torch.empty(q.shape[0], s_q, 128, 512, dtype=q.dtype, device=device)
     lse = torch.empty(q.shape[0], s_q, 128, dtype=torch.float32, device=device)
-    meta, ns = mla.mla_get_metadata(sl, s_q, 128, causal=causal)
+    meta, ns = mla.mla_get_metadata(sl, s_q, 128, **meta_args)
     stream = torch.cuda.current_stream(device)
+    dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8, indices=idx)
 
     def step():
-        m, n = mla.mla_get_metadata(sl, s_q, 128, causal=causal, num_sm_parts=meta.parts)
-        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
-                                    out=out, lse=lse)
+        m, n = mla.mla_get_metadata(sl, s_q, 128, num_sm_parts=meta.parts, **meta_args)
+        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
 
     # correctness gate before timing: device status must be clean
     step()
@@ -218,13 +262,11 @@ def run_ours(args, w, rank, world, device):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.roofline_steps)]
     for k in range(args.roofline_steps):
         ev[k][0].record(stream)
-        m, n = mla.mla_get_metadata(sl, s_q, 128, causal=causal, num_sm_parts=meta.parts)
+        m, n = mla.mla_get_metadata(sl, s_q, 128, num_sm_parts=meta.parts, **meta_args)
         ev[k][1].record(stream)
-        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
-                               out=out, lse=lse)
+        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
         ev[k][2].record(stream)
-        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, softmax_scale=case.softmax_scale, causal=causal,
-                               out=out, lse=lse)
+        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
         ev[k][3].record(stream)
     torch.cuda.synchronize(device)
     t_meta = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
@@ -235,19 +277,25 @@ def run_ours(args, w, rank, world, device):
     e2e = None
     if not args.no_e2e:
         qh = q.cpu().pin_memory()
-        bth = case.block_table.pin_memory()
-        slh = case.cache_seqlens.pin_memory()
+        host_in = [qh]
+        dev_in = [torch.empty_like(q)]
+        for t_dev in (bt, sl, idx):
+            if t_dev is not None:
+                host_in.append(t_dev.cpu().pin_memory())
+                dev_in.append(torch.empty_like(t_dev))
         outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        qd, btd, sld = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
 
         def e2e_step():
-            qd.copy_(qh, non_blocking=True)
-            btd.copy_(bth, non_blocking=True)
-            sld.copy_(slh, non_blocking=True)
-            m, n = mla.mla_get_metadata(sld, s_q, 128, causal=causal, num_sm_parts=meta.parts)
-            mla.mla_decode_with_kvcache(qd, kv, btd, sld, 512, m, n, softmax_scale=case.softmax_scale,
-                                        causal=causal, out=out, lse=lse)
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            it_ = iter(dev_in[1:])
+            btd = next(it_) if bt is not None else None
+            sld = next(it_) if sl is not None else None
+            idxd = next(it_) if idx is not None else None
+            m, n = mla.mla_get_metadata(sld, s_q, 128, num_sm_parts=meta.parts, **meta_args)
+            mla.mla_decode_with_kvcache(dev_in[0], kv, btd, sld, 512, m, n, out=out, lse=lse,
+                                        softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8, indices=idxd)
             outh.copy_(out, non_blocking=True)
             lseh.copy_(lse, non_blocking=True)
 
@@ -270,7 +318,7 @@ def run_ours(args, w, rank, world, device):
             t = torch.tensor([t_e2e], dtype=torch.float64, device=device)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             t_e2e = float(t.item())
-        h2d = qh.numel() * qh.element_size() + bth.numel() * 4 + slh.numel() * 4
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = outh.numel() * outh.element_size() + lseh.numel() * 4
         e2e = {"value": round(world * flops / t_e2e / 1e12, 3), "unit": "TFLOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -323,14 +371,14 @@ def main():
         achieved = r["algo_bytes"] / r["t_dec"] / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                "kernel": "mla_decode_dense_kernel", "peak_source": f"{peak_src} hbm_gbs"}
+                "kernel": "mla_decode_kernel", "peak_source": f"{peak_src} hbm_gbs"}
     else:
         achieved = r["flops"] / r["t_dec"] / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": round(achieved / tc_peak, 4), "traffic": None,
-                "kernel": "mla_decode_dense_kernel", "peak_source": f"{peak_src} bf16_tflops"}
+                "kernel": "mla_decode_kernel", "peak_source": f"{peak_src} bf16_tflops"}
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and w["kind"] == "dense":
         cpu_case = r["case"]
         rate, desc, _, _ = oracle_rate(cpu_case, r["seqlens"], args.cpu_budget)
         cpu = {"value": round(rate / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
@@ -338,10 +386,13 @@ def main():
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["kind"] == "dense" else "fp8-e4m3 cache, fp16/bf16 MMA",
+        "data": "synthetic",
         "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": 128, "d_qk": 576,
                    "d_v": 512, "page_block": 64, "causal": w["causal"],
-                   "seqlens": (f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
+                   "cache": {"dense": "bf16", "fp8": "fp8-656B", "sparse": "fp8-656B"}[w["kind"]],
+                   "seqlens": (f"topk {w['topk']} of {SPARSE_TOKENS} per request, 5% -1" if w["kind"] == "sparse"
+                               else f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
                                else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),
                    "parallelism": f"replicas x{world}", "num_sm_parts": r["parts"],
                    "l2": "inputs larger than L2 (KV cache %.0f MB per replica)" % (r["kv_bytes"] / 1e6)},

@@ -71,21 +71,22 @@ constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
 constexpr int kSlot = 4 * kKChunk + kRChunk;
 constexpr int kThreads = 384;
-constexpr int kSoftmaxWarps = 8;
+constexpr int kEWarps = 4;                 // warps 4-7: exponentiate and send
+constexpr int kPWarps = 4;                 // warps 8-11: receive, form P, epilogue
 constexpr int kDequantWarps = 2;           // warps 2-3 (FP8 caches)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
 constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
 constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
-constexpr uint32_t kXBytes = kXE + 128 * 4;             // + m_r per row
+constexpr uint32_t kXM = kXE;                           // + m_r per row (fp32)
+constexpr uint32_t kXMask = kXM + 128 * 4;              // + validity mask of the tile (64 bits)
+constexpr uint32_t kXBytes = kXMask + 16;
 constexpr uint32_t kXStride = 17 * 1024;
-constexpr uint32_t kSoftmaxBar = 1;                     // named barrier of the 256 softmax threads
-constexpr uint32_t kPairBar = 2;                        // + quadrant: the two warps of one lane quadrant
+constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
 constexpr uint32_t kRawLat = 64 * 256;     // this CTA's 256 e4m3 per token
 constexpr uint32_t kRawSc = 64 * 16;       // the 4 scales per token
 constexpr uint32_t kRawRope = 64 * 64;     // this CTA's 32 RoPE dims per token (sparse staging)
-constexpr uint32_t kRawSlot = kRawLat + kRawSc + kRawRope;
 constexpr int kRawNS = 2;
 
 // per-mode layout (offsets from a 1024-B aligned base) and barrier indices
@@ -96,18 +97,19 @@ struct Cfg {
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
   static constexpr int kNS = kFp8 ? 3 : 4;               // KV ring slots (tiles)
   static constexpr int kPrefetch = kNS;                  // dense: tiles ahead of the ring prefetched into L2
+  static constexpr uint32_t kRawSlot = kRawLat + kRawSc + (kSparse ? kRawRope : 0);
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
-  static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
-  static constexpr uint32_t OFF_P = OFF_XS + kXStride;   // 128 rows x 64 bf16
+  static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own messages (2 tiles), staged for the copy
+  static constexpr uint32_t OFF_P = OFF_XS + 2 * kXStride;  // 128 rows x 64 bf16
   static constexpr uint32_t OFF_QR = OFF_P + 128 * 128;  // 32 RoPE dims of Q: 128 rows x 64 B
   static constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
   static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlot;
-  static constexpr uint32_t OFF_MX = OFF_RAW + (kFp8 ? kRawNS * kRawSlot : 0);  // row max / row sum halves
-  static constexpr uint32_t OFF_BAR = OFF_MX + 3 * 2 * 128 * 4;
+  static constexpr uint32_t OFF_BAR = OFF_RAW + (kFp8 ? kRawNS * kRawSlot : 0);
   static constexpr uint32_t B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1,
                             B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2,
                             B_PEMPTY = B_PFULL + 1, B_OEMPTY = B_PEMPTY + 1, B_XFULL = B_OEMPTY + 1,
-                            B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_RFULL = B_DRAIN + 1,
+                            B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_XSFREE = B_DRAIN + 1,
+                            B_XSFULL = B_XSFREE + 2, B_RFULL = B_XSFULL + 2,
                             B_REMPTY = B_RFULL + kRawNS, B_COUNT = B_REMPTY + kRawNS;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem slot, abort flag, ok flag
   static constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -228,17 +230,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_FULL + s), kFp8 ? 1 + kDequantWarps : 1);
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    mbar_init(bar(C::B_QFULL), kSoftmaxWarps + 1);  // softmax warps (latent into TMEM) + RoPE TMA
+    mbar_init(bar(C::B_QFULL), kEWarps + 1);  // E warps (latent into TMEM) + RoPE TMA
     mbar_init(bar(C::B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_SEMPTY + s), kSoftmaxWarps);
+      mbar_init(bar(C::B_SEMPTY + s), kEWarps);
+      mbar_init(bar(C::B_XSFREE + s), kPWarps);  // P warps have read XS[s]
+      mbar_init(bar(C::B_XSFULL + s), 1);        // E warps have staged XS[s]
     }
-    mbar_init(bar(C::B_PFULL), kSoftmaxWarps);
+    mbar_init(bar(C::B_PFULL), kPWarps);
     mbar_init(bar(C::B_PEMPTY), 1);
-    mbar_init(bar(C::B_OEMPTY), kSoftmaxWarps);
+    mbar_init(bar(C::B_OEMPTY), kPWarps);
     mbar_init(bar(C::B_XFULL), 1);              // own expect_tx + the peer's copied bytes
-    mbar_init(bar(C::B_XEMPTY), kSoftmaxWarps);  // one arrive per peer softmax warp
+    mbar_init(bar(C::B_XEMPTY), kPWarps);  // one arrive per peer P warp
     mbar_init(bar(C::B_DRAIN), 1);
     for (int s = 0; s < kRawNS; ++s) {
       mbar_init(bar(C::B_RFULL + s), 1);
@@ -318,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // raw e4m3 + scales into the staging ring, converted by the dequant warps
             const int rs = g % kRawNS;
             if (!wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
-            const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+            const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
             mbar_arrive_expect_tx(bar(C::B_RFULL + rs), kRawLat + kRawSc);
             tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), 256 * (int)rank, page * kTile, pol_kv);
             tma_load_2d(raw + kRawLat, &tm_sc, bar(C::B_RFULL + rs), 512, page * kTile, pol_kv);
@@ -343,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // sparse: one bulk copy per valid row and field, issued by the whole warp
           const int rs = g % kRawNS;
           if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
-          const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+          const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
           const int32_t* irow = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
           int idx[2];
           bool okr[2];
@@ -410,9 +414,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           failed = true;
           break;
         }
-        const uint32_t raw = sb + C::OFF_RAW + rs * kRawSlot;
+        const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
         const uint32_t slot = sb + C::OFF_RING + s * kSlot;
-        const float* scales = reinterpret_cast<const float*>(smem + C::OFF_RAW + rs * kRawSlot + kRawLat);
+        const float* scales = reinterpret_cast<const float*>(smem + C::OFF_RAW + rs * C::kRawSlot + kRawLat);
         // 64 rows x 32 units of 8 values; consecutive lanes take consecutive
         // units of one row (conflict-free 8-B loads, 16-B swizzled stores)
 #pragma unroll 4
@@ -545,169 +549,177 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     umma_commit(bar(C::B_DRAIN));
     const uint64_t t_0 = globaltimer();
     while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t_0 < 200000000ull) {}
-  } else if (ok && warp >= 4) {
-    // ---------------- softmax / exchange / epilogue ----------------
-    const int q4 = warp & 3;                              // TMEM lane quadrant
-    const int c = (warp - 4) >> 2;                        // score column half
-    const int h = 32 * q4 + lane;                         // head = TMEM lane
-    const int sid = threadIdx.x - 128;                    // 0..255 among softmax threads
-    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t xr_row = sb + C::OFF_XR + h * 128;     // same offsets in both CTAs
-    const uint32_t xs_row = sb + C::OFF_XS + h * 128;
+  } else if (ok && warp >= 4 && warp < 8) {
+    // ---------------- E warps: S -> E = exp2(x - m_own), stage, send ----------------
+    const int h = 32 * (warp - 4) + lane;                 // head = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
     const uint32_t xr_remote = mapa(sb + C::OFF_XR, peer);
     const uint32_t xfull_remote = mapa(bar(C::B_XFULL), peer);
-    const uint32_t xempty_remote = mapa(bar(C::B_XEMPTY), peer);
-    const uint32_t p_row = sb + C::OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
-    float* mx = reinterpret_cast<float*>(smem + C::OFF_MX);  // [tile parity][half][row]
-    float* lx = mx + 2 * 256;                                // [half][row]
-    const float* xr_m = reinterpret_cast<const float*>(smem + C::OFF_XR + kXE);
-    float* xs_m = reinterpret_cast<float*>(smem + C::OFF_XS + kXE);
     const float sl2 = p.scale_log2;
-    const uint32_t pair_bar = kPairBar + q4;
-
     // copy this CTA's 256 latent dims of every head's query row into TMEM
-    // (each of the two warps of a quadrant copies 128 of them)
     auto load_q = [&](const Piece& q_pc, int q_idx) -> bool {
       if (q_idx > 0 && !warp_ok(wait(bar(C::B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
       const int b = q_pc.v % p.batch, i = q_pc.v / p.batch;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const uint16_t*>(p.q) + ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank + 128 * c);
-      uint32_t r[64];
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
+                                                        ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint4 x = __ldg(src + k);
-        r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
-      }
-      if constexpr (kFp8) {  // latent operands of FP8 caches are fp16
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[64];
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
-          r[k] = pack_f16x2_sat(__uint_as_float(r[k] << 16), __uint_as_float(r[k] & 0xFFFF0000u));
+        for (int k = 0; k < 16; ++k) {
+          const uint4 x = __ldg(src + 16 * half + k);
+          r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
+        }
+        if constexpr (kFp8) {  // latent operands of FP8 caches are fp16
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            r[k] = pack_f16x2_sat(__uint_as_float(r[k] << 16), __uint_as_float(r[k] & 0xFFFF0000u));
+        }
+        tc_fence_after();
+        tmem_st32(tl + kColQ + 64u * half, r);
+        tmem_st32(tl + kColQ + 64u * half + 32u, r + 32);
       }
-      tc_fence_after();
-      tmem_st32(tl + kColQ + 64u * c, r);
-      tmem_st32(tl + kColQ + 64u * c + 32u, r + 32);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_QFULL));
       return true;
     };
-    // Tile gg: read this warp's 32 partial-score columns from TMEM, E_r =
-    // exp2(x - m_r) with x = S_r * scale * log2e and m_r the partial row max
-    // over the valid tokens (vmask; masked tokens get E = 0), kept as fp16
-    // pairs in `e`; stage E_r and m_r and copy them to the peer.
-    auto send_partial = [&](int gg, uint32_t vm, uint32_t* e, float& m_own) -> bool {
-      const int sbuf = gg & 1;
-      if (!warp_ok(wait(bar(C::B_SFULL + sbuf), (gg >> 1) & 1, guard))) return false;
-      tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld32(tl + kColS + 64u * sbuf + 32u * c, sr);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + sbuf));
-      float x[32];
-      float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        x[k] = (vm >> k) & 1u ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
-        x[k + 1] = (vm >> (k + 1)) & 1u ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
-        m0 = fmaxf(m0, x[k]);
-        m1 = fmaxf(m1, x[k + 1]);
-      }
-      float* mxg = mx + (gg & 1) * 256;
-      mxg[c * 128 + h] = fmaxf(m0, m1);
-      named_sync(pair_bar, 64);
-      m_own = fmaxf(mxg[h], mxg[128 + h]);
-      const float mref = m_own == -INFINITY ? 0.f : m_own;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) e[u] = pack_f16x2(exp2_approx(x[2 * u] - mref), exp2_approx(x[2 * u + 1] - mref));
-      // the peer has consumed the previous message: staging and its receive
-      // buffer are free
-      if (!warp_ok(wait_cluster(bar(C::B_XEMPTY), (gg & 1) ^ 1, guard))) return false;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_shared_v4(xs_row + (((4 * c + u) ^ (h & 7)) << 4), e[4 * u], e[4 * u + 1], e[4 * u + 2], e[4 * u + 3]);
-      if (c == 0) xs_m[h] = m_own;
-      fence_proxy_async_smem();
-      named_sync(kSoftmaxBar, 256);
-      if (sid == 0) bulk_copy_to_peer(xr_remote, sb + C::OFF_XS, kXBytes, xfull_remote);
-      return true;
-    };
-
     PieceIter it(p, part);
-    Piece pc, nx;
+    Piece pc;
     int g = 0, qi = 0;
     bool failed = false;
-    bool have = it.next(pc);
-    if (have) failed = !load_q(pc, qi++);
-    uint32_t cur[16];   // own E of the tile being finished (fp16 pairs)
-    float m_cur = -INFINITY;
-    while (have && !failed) {
-      const int b = pc.v % p.batch, i = pc.v / p.batch;
-      float m = -INFINITY, l_half = 0.f;
-      uint64_t vm_cur = tile_mask<kSparse>(p, pc.v, pc.t0, pc.len, rank == 0 && sid < 32);
-      if (!send_partial(g, (uint32_t)(vm_cur >> (32 * c)), cur, m_cur)) { failed = true; break; }
+    while (!failed && it.next(pc)) {
+      if (!load_q(pc, qi++)) break;
+      uint64_t vm_next = tile_mask<kSparse>(p, pc.v, pc.t0, pc.len, rank == 0 && warp == 4);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const uint64_t vm = vm_cur;
-        // (1) receive the peer's E and m of tile g
-        if (sid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
-        if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
-        uint32_t ep[16];
+        const uint64_t vm = vm_next;
+        if (t + 1 < pc.t1) vm_next = tile_mask<kSparse>(p, pc.v, t + 1, pc.len, rank == 0 && warp == 4);
+        const int sbuf = g & 1;
+        if (!warp_ok(wait(bar(C::B_SFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tl + kColS + 64u * sbuf, sr);
+        tmem_ld32(tl + kColS + 64u * sbuf + 32u, sr + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + sbuf));
+        float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 o = ld_shared_v4f(xr_row + (((4 * c + u) ^ (h & 7)) << 4));
+        for (int k = 0; k < 64; k += 2) {
+          const float a = (vm >> k) & 1ull ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
+          const float b2 = (vm >> (k + 1)) & 1ull ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
+          sr[k] = __float_as_uint(a);
+          sr[k + 1] = __float_as_uint(b2);
+          m0 = fmaxf(m0, a);
+          m1 = fmaxf(m1, b2);
+        }
+        const float m_own = fmaxf(m0, m1);
+        const float mref = m_own == -INFINITY ? 0.f : m_own;
+        uint32_t e[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          e[u] = pack_f16x2(exp2_approx(__uint_as_float(sr[2 * u]) - mref),
+                            exp2_approx(__uint_as_float(sr[2 * u + 1]) - mref));
+        // XS[g&1] is free once this CTA's P warps have read tile g-2 from it,
+        // and the peer's receive buffer once the peer has read tile g-1
+        if (!warp_ok(wait(bar(C::B_XSFREE + sbuf), ((g >> 1) & 1) ^ 1, guard)) ||
+            !warp_ok(wait_cluster(bar(C::B_XEMPTY), (g & 1) ^ 1, guard))) {
+          failed = true;
+          break;
+        }
+        const uint32_t xs = sb + C::OFF_XS + sbuf * kXStride;
+        const uint32_t xs_row = xs + h * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(xs_row + ((u ^ (h & 7)) << 4), e[4 * u], e[4 * u + 1], e[4 * u + 2], e[4 * u + 3]);
+        reinterpret_cast<float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h] = m_own;
+        if (h == 0) *reinterpret_cast<uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask) = vm;
+        fence_proxy_async_smem();
+        named_sync(kEBar, 128);
+        if (h == 0) {
+          bulk_copy_to_peer(xr_remote, xs, kXBytes, xfull_remote);
+          mbar_arrive(bar(C::B_XSFULL + sbuf));
+        }
+      }
+    }
+  } else if (ok && warp >= 8) {
+    // ---------------- P warps: receive, P = E_own * E_peer * 2^(m_own + m_peer - m_ref) ----------------
+    const int h = 32 * (warp - 8) + lane;                 // head = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 8)) << 16);
+    const uint32_t xr_row = sb + C::OFF_XR + h * 128;
+    const uint32_t xempty_remote = mapa(bar(C::B_XEMPTY), peer);
+    const uint32_t p_row = sb + C::OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
+    const float* xr_m = reinterpret_cast<const float*>(smem + C::OFF_XR + kXM);
+    const int pid = threadIdx.x - 256;                    // 0..127 among P threads
+    PieceIter it(p, part);
+    Piece pc;
+    int g = 0, pcount = 0;
+    bool failed = false;
+    while (!failed && it.next(pc)) {
+      const int b = pc.v % p.batch, i = pc.v / p.batch;
+      float m = -INFINITY, l = 0.f;
+      for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+        const int sbuf = g & 1;
+        // (1) the peer's E and m of tile g
+        if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
+        if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
+        uint32_t ep[32], eo[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
           ep[4 * u] = __float_as_uint(o.x); ep[4 * u + 1] = __float_as_uint(o.y);
           ep[4 * u + 2] = __float_as_uint(o.z); ep[4 * u + 3] = __float_as_uint(o.w);
         }
         const float m_peer = xr_m[h];
-        // the loads above have returned their values, so a relaxed arrive is
-        // enough to let the peer overwrite the buffer
+        // loads returned: a relaxed arrive lets the peer overwrite the buffer
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote);
-        uint32_t eo[16];
+        // (2) this CTA's own E and m of tile g, staged by the E warps
+        if (!warp_ok(wait(bar(C::B_XSFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
+        const uint32_t xs_row = sb + C::OFF_XS + sbuf * kXStride + h * 128;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) eo[u] = cur[u];
-        const float m_mine = m_cur;
-        // (2) exponentiate and send tile g+1 (same piece)
-        if (t + 1 < pc.t1) {
-          vm_cur = tile_mask<kSparse>(p, pc.v, t + 1, pc.len, rank == 0 && sid < 32);
-          if (!send_partial(g + 1, (uint32_t)(vm_cur >> (32 * c)), cur, m_cur)) { failed = true; break; }
+        for (int u = 0; u < 8; ++u) {
+          const float4 o = ld_shared_v4f(xs_row + ((u ^ (h & 7)) << 4));
+          eo[4 * u] = __float_as_uint(o.x); eo[4 * u + 1] = __float_as_uint(o.y);
+          eo[4 * u + 2] = __float_as_uint(o.z); eo[4 * u + 3] = __float_as_uint(o.w);
         }
-        // (3) P of tile g: E_0 * E_1 * 2^(m_0 + m_1 - m_ref), lazy rescale
-        // against the running reference max (P stays <= 256)
-        const float mt = m_mine + m_peer;  // upper bound of the tile's scaled row max
+        const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h];
+        const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_XSFREE + sbuf));
+        // (3) P with lazy rescale against the running reference max (P <= 256)
+        const float mt = m_own + m_peer;  // upper bound of the tile's scaled row max
         const float m_new = fmaxf(m, mt);
         const bool resc = m_new > m + 8.0f;
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? exp2_approx(m - m_new) : 1.0f;
         const float cf = mt == -INFINITY ? 0.f : exp2_approx(mt - (m_use == -INFINITY ? 0.f : m_use));
         float rs0 = 0.f, rs1 = 0.f;
-        uint32_t pw[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 32; ++u) {
           const float2 fo = unpack_f16x2(eo[u]), fq = unpack_f16x2(ep[u]);
           const float a0 = fo.x * fq.x * cf;
           const float a1 = fo.y * fq.y * cf;
           rs0 += a0;
           rs1 += a1;
-          pw[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+          ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
         }
-        l_half = l_half * alpha + (rs0 + rs1);
+        l = l * alpha + (rs0 + rs1);
         m = m_use;
         // the previous P . V has finished: P buffer and O are free
         if (g > 0 && !warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, resc) && t != pc.t0) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 8; ++cc) {
             uint32_t r[32];
-            const uint32_t col = 128u * c + 32u * cc;
-            tmem_ld32(tl + col, r);
+            tmem_ld32(tl + 32u * cc, r);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-            tmem_st32(tl + col, r);
+            tmem_st32(tl + 32u * cc, r);
           }
           tmem_wait_st();
         }
@@ -715,42 +727,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
           // turn into NaN inside P . V (the dequant warps do this for FP8 rows)
           const uint32_t slot = sb + C::OFF_RING + (g % NS) * kSlot;
-          for (int e2 = sid; e2 < 64 * 32; e2 += 256) {
+          for (int e2 = pid; e2 < 64 * 32; e2 += 128) {
             const int row = e2 >> 5, u = e2 & 31;
             if (!((vm >> row) & 1ull))
               st_shared_v4(slot + (u >> 3) * kKChunk + row * 128 + (u & 7) * 16, 0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(p_row + (((4 * c + u) ^ (h & 7)) << 4), pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(p_row + ((u ^ (h & 7)) << 4), ep[4 * u], ep[4 * u + 1], ep[4 * u + 2], ep[4 * u + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PFULL));
       }
       if (failed) break;
-      // the next piece's Q goes into TMEM before this piece's epilogue, so
-      // its first QK^T overlaps the epilogue
-      const bool have_next = it.next(nx);
-      if (have_next && !load_q(nx, qi++)) { failed = true; break; }
       // ---- epilogue of the piece: O / l -> out (single piece) or partial ----
-      lx[c * 128 + h] = l_half;
-      named_sync(pair_bar, 64);
-      const float l = lx[h] + lx[128 + h];
       if (!warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       const int64_t row = (int64_t)(b * p.s_q + i) * 128 + h;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 8; ++cc) {
         uint32_t r[32];
-        const int col = 128 * c + 32 * cc;
-        tmem_ld32(tl + (uint32_t)col, r);
+        tmem_ld32(tl + 32u * cc, r);
         tmem_wait_ld();
         if (pc.fin) {
-          OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + col;
+          OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + 32 * cc;
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
             uint4 w;
@@ -762,7 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + k) = w;
           }
         } else {
-          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + col;
+          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * cc;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<float4*>(dst + k) =
@@ -770,15 +774,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             __uint_as_float(r[k + 2]) * inv_l, __uint_as_float(r[k + 3]) * inv_l);
         }
       }
-      if (rank == 0 && c == 0) {
+      if (rank == 0) {
         if (pc.fin) p.lse[row] = lse;
         else p.lse_part[(int64_t)pc.split * 128 + h] = lse;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_OEMPTY));
-      pc = nx;
-      have = have_next;
+      ++pcount;
     }
   }
 
