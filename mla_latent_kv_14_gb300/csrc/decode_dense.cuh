@@ -96,7 +96,6 @@ struct Cfg {
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
   static constexpr int kNS = kFp8 ? 3 : 4;               // KV ring slots (tiles)
-  static constexpr int kPrefetch = kNS;                  // dense: tiles ahead of the ring prefetched into L2
   static constexpr uint32_t kRawSlot = kRawLat + kRawSc + (kSparse ? kRawRope : 0);
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
   static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own messages (2 tiles), staged for the copy
@@ -110,7 +109,8 @@ struct Cfg {
                             B_PEMPTY = B_PFULL + 1, B_OEMPTY = B_PEMPTY + 1, B_XFULL = B_OEMPTY + 1,
                             B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_XSFREE = B_DRAIN + 1,
                             B_XSFULL = B_XSFREE + 2, B_RFULL = B_XSFULL + 2,
-                            B_REMPTY = B_RFULL + kRawNS, B_COUNT = B_REMPTY + kRawNS;
+                            B_REMPTY = B_RFULL + kRawNS, B_DRAIN2 = B_REMPTY + kRawNS,
+                            B_COUNT = B_DRAIN2 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem slot, abort flag, ok flag
   static constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -155,43 +155,99 @@ struct PieceIter {
 
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
 
-// valid tokens of tile t of a dense request (0 if its page is out of range)
-__device__ __forceinline__ int dense_valid(const DecodeParams& p, int b, int t, int len) {
+// Tile validity masks, computed by a whole warp, bit k = token 64t+k.
+// Dense: the first min(len - 64t, 64) tokens, or none if the tile's page is
+// out of range (reported). Sparse: the index-list entries in [0, num_rows);
+// -1 is skipped silently, other out-of-range entries are reported.
+// The global loads behind a mask (block-table entries, index-list entries) are
+// issued well before the mask is needed: a dense stream loads the pages of 32
+// tiles per warp-wide load, one block ahead; a sparse stream loads the indices
+// of tile t+2 while tile t is processed.
+__device__ __forceinline__ int load_pages32(const DecodeParams& p, int b, int t) {
+  const int tt = t + (int)(threadIdx.x & 31);
+  return tt < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + tt) : -1;
+}
+__device__ __forceinline__ uint64_t dense_mask(const DecodeParams& p, int page, int t, int len, bool report) {
   int nv = len - t * kTile;
   nv = nv > kTile ? kTile : nv;
-  const int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-  return (page < 0 || page >= p.num_blocks) ? 0 : nv;
+  if (page < 0 || page >= p.num_blocks) {
+    if (report && (threadIdx.x & 31) == 0) atomicOr(p.status, STATUS_INDEX);
+    nv = 0;
+  }
+  return nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+}
+__device__ __forceinline__ void sparse_fetch(const DecodeParams& p, int v, int t, int& i0, int& i1) {
+  const int b = v % p.batch, i = v / p.batch;
+  const int32_t* row = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
+  const int k = 64 * t + (int)(threadIdx.x & 31);
+  i0 = k < p.topk ? __ldg(row + k) : -1;
+  i1 = k + 32 < p.topk ? __ldg(row + k + 32) : -1;
+}
+__device__ __forceinline__ uint64_t sparse_mask(const DecodeParams& p, int i0, int i1, bool report) {
+  const bool ok0 = i0 >= 0 && (int64_t)i0 < p.num_rows;
+  const bool ok1 = i1 >= 0 && (int64_t)i1 < p.num_rows;
+  const bool bad = (i0 != -1 && !ok0) || (i1 != -1 && !ok1);
+  const uint32_t lo = __ballot_sync(0xffffffffu, ok0), hi = __ballot_sync(0xffffffffu, ok1);
+  if (report && __any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(p.status, STATUS_INDEX);
+  return (uint64_t)lo | ((uint64_t)hi << 32);
 }
 
-// Validity of the 64 tokens of tile t as a bit mask (bit k = token 64t+k),
-// computed by a whole warp. Dense: the first nv tokens (a tile whose page is
-// out of range is empty). Sparse: the index-list entries in [0, num_rows);
-// -1 is silently skipped, other out-of-range entries are reported.
-template <bool kSparse>
-__device__ __forceinline__ uint64_t tile_mask(const DecodeParams& p, int v, int t, int len, bool report) {
-  const int lane = threadIdx.x & 31;
-  if constexpr (!kSparse) {
-    const int b = v % p.batch;
-    const int nv = dense_valid(p, b, t, len);
-    if (report && nv == 0 && lane == 0) atomicOr(p.status, STATUS_INDEX);
-    return nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
-  } else {
-    const int b = v % p.batch, i = v / p.batch;
-    const int32_t* row = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
-    uint32_t half[2];
-    bool bad = false;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int k = 64 * t + 32 * hh + lane;
-      const int idx = k < p.topk ? __ldg(row + k) : -1;
-      const bool ok = idx >= 0 && (int64_t)idx < p.num_rows;
-      bad |= (idx != -1 && !ok);
-      half[hh] = __ballot_sync(0xffffffffu, ok);
-    }
-    if (report && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, STATUS_INDEX);
-    return (uint64_t)half[0] | ((uint64_t)half[1] << 32);
+// The pages of one dense request seen through a 64-tile window: lane i holds
+// the page of tile base+i (cur) and base+32+i (nxt); moving the window loads
+// the block after next, 32 tiles before it is used.
+struct PageWindow {
+  int b, base, cur, nxt;
+  __device__ __forceinline__ void start(const DecodeParams& p, int b_, int t0) {
+    b = b_;
+    base = t0;
+    cur = load_pages32(p, b, t0);
+    nxt = load_pages32(p, b, t0 + 32);
   }
-}
+  __device__ __forceinline__ void advance(const DecodeParams& p, int t) {
+    while (t - base >= 32) {
+      base += 32;
+      cur = nxt;
+      nxt = load_pages32(p, b, base + 32);
+    }
+  }
+  // t - base in [0, 64); every lane calls it with the same t
+  __device__ __forceinline__ int get(int t) const {
+    const int d = t - base;
+    const int a = __shfl_sync(0xffffffffu, cur, d & 31);
+    const int c = __shfl_sync(0xffffffffu, nxt, d & 31);
+    return d < 32 ? a : c;
+  }
+};
+
+// masks of consecutive tiles t0, t0+1, ... of one piece (one call per tile)
+template <bool kSparse>
+struct MaskStream {
+  int v, len;
+  PageWindow w;
+  int a0, a1, c0, c1;  // sparse: indices of the next two tiles
+  __device__ __forceinline__ void start(const DecodeParams& p, const Piece& pc) {
+    v = pc.v;
+    len = pc.len;
+    if constexpr (kSparse) {
+      sparse_fetch(p, v, pc.t0, a0, a1);
+      sparse_fetch(p, v, pc.t0 + 1, c0, c1);
+    } else {
+      w.start(p, v % p.batch, pc.t0);
+    }
+  }
+  __device__ __forceinline__ uint64_t next(const DecodeParams& p, int t, bool report) {
+    if constexpr (kSparse) {
+      const uint64_t m = sparse_mask(p, a0, a1, report);
+      a0 = c0;
+      a1 = c1;
+      sparse_fetch(p, v, t + 2, c0, c1);
+      return m;
+    } else {
+      w.advance(p, t);
+      return dense_mask(p, w.get(t), t, len, report);
+    }
+  }
+};
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
   uint32_t r;
@@ -206,6 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const DecodeParams p) {
   using C = Cfg<kMode>;
   constexpr bool kFp16 = C::kFp16, kFp8 = C::kFp8, kSparse = C::kSparse;
+  constexpr bool kSplitIssue = !kFp8;  // warp 2 is free to issue P . V unless it dequantises
   constexpr int NS = C::kNS;
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
@@ -221,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
   volatile uint32_t* ok_flag = misc + 2;
-  const Guard guard{abort_flag, p.status, 1500000000ull};
+  const Guard guard{abort_flag, p.status, kWaitLimitCycles};
 
   const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
   if (threadIdx.x == 0) {
@@ -244,6 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_XFULL), 1);              // own expect_tx + the peer's copied bytes
     mbar_init(bar(C::B_XEMPTY), kPWarps);  // one arrive per peer P warp
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_DRAIN2), 1);
     for (int s = 0; s < kRawNS; ++s) {
       mbar_init(bar(C::B_RFULL + s), 1);
       mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
@@ -285,19 +343,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int last_rg[kRawNS] = {-1, -1};
     int q_last = -1;
     bool stop = false;
-    auto page_of = [&](int b, int t) {
-      int page = t < p.max_blocks ? p.block_table[(int64_t)b * p.max_blocks + t] : -1;
-      return (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the consumers
+    // block-table entries are loaded one iteration before they are used
+    auto raw_page = [&](int b, int t) {
+      return t < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + t) : -1;
     };
-    auto prefetch_tile = [&](int page) {
-      if constexpr (kFp8) {
-        tma_prefetch_2d(&tm_kv, 256 * (int)rank, page * kTile);
-      } else {
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) tma_prefetch_2d(&tm_kv, 256 * (int)rank + 64 * ci, page * kTile);
-        tma_prefetch_2d(&tm_kvr, xr, page * kTile);
-      }
-    };
+    auto sane = [&](int page) { return (page < 0 || page >= p.num_blocks) ? 0 : page; };  // bad pages are masked
     while (!stop && it.next(pc)) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       if (lane == 0) {
@@ -311,13 +361,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kSparse && !warp_ok(!stop)) stop = true;
       if (stop) break;
       ++qn;
-      if constexpr (!kSparse)
-        for (int t = pc.t0; t < pc.t0 + NS && t < pc.t1; ++t) prefetch_tile(page_of(b, t));
+      int pg_next = 0;               // dense: page of tile t, loaded one tile ahead
+      int n0 = 0, n1 = 0;            // sparse: indices of tile t, loaded ahead
+      if constexpr (!kSparse) {
+        pg_next = raw_page(b, pc.t0);
+      } else {
+        sparse_fetch(p, pc.v, pc.t0, n0, n1);
+      }
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const int s = g % NS;
         if constexpr (!kSparse) {
-          const int page = page_of(b, t);
-          if (t + C::kPrefetch < pc.t1) prefetch_tile(page_of(b, t + C::kPrefetch));
+          const int page = sane(pg_next);
+          pg_next = raw_page(b, t + 1);
           if constexpr (kFp8) {
             // raw e4m3 + scales into the staging ring, converted by the dequant warps
             const int rs = g % kRawNS;
@@ -336,10 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), 528 + 64 * (int)rank, page * kTile, pol_kv);
           } else {
             mbar_arrive_expect_tx(bar(C::B_FULL + s), kSlot);
-#pragma unroll
-            for (int ci = 0; ci < 4; ++ci)
-              tma_load_2d(slot + ci * kKChunk, &tm_kv, bar(C::B_FULL + s), 256 * (int)rank + 64 * ci, page * kTile,
-                          pol_kv);
+            tma_load_3d(slot, &tm_kv, bar(C::B_FULL + s), 0, page * kTile, 4 * (int)rank, pol_kv);
             tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), xr, page * kTile, pol_kv);
           }
           last_g[s] = g;
@@ -348,14 +400,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int rs = g % kRawNS;
           if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
           const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
-          const int32_t* irow = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
-          int idx[2];
+          const int idx[2] = {n0, n1};
+          if (t + 1 < pc.t1) sparse_fetch(p, pc.v, t + 1, n0, n1);  // consumed next tile
           bool okr[2];
           int nvalid = 0;
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const int k = 64 * t + 32 * hh + lane;
-            idx[hh] = k < p.topk ? __ldg(irow + k) : -1;
             okr[hh] = idx[hh] >= 0 && (int64_t)idx[hh] < p.num_rows;
             nvalid += __popc(__ballot_sync(0xffffffffu, okr[hh]));
           }
@@ -383,17 +433,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int s = 0; s < NS; ++s)
         if (last_g[s] >= 0) {
-          const uint64_t t_0 = globaltimer();
-          while (!mbar_try_wait(bar(C::B_FULL + s), (last_g[s] / NS) & 1) && globaltimer() - t_0 < 200000000ull) {}
+          const uint64_t t_0 = cycles();
+          while (!mbar_try_wait(bar(C::B_FULL + s), (last_g[s] / NS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
         }
       for (int s = 0; s < kRawNS; ++s)
         if (last_rg[s] >= 0) {
-          const uint64_t t_0 = globaltimer();
-          while (!mbar_try_wait(bar(C::B_RFULL + s), (last_rg[s] / kRawNS) & 1) && globaltimer() - t_0 < 200000000ull) {}
+          const uint64_t t_0 = cycles();
+          while (!mbar_try_wait(bar(C::B_RFULL + s), (last_rg[s] / kRawNS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
         }
       if (q_last >= 0) {
-        const uint64_t t_0 = globaltimer();
-        while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && globaltimer() - t_0 < 200000000ull) {}
+        const uint64_t t_0 = cycles();
+        while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && cycles() - t_0 < kDrainLimitCycles) {}
       }
     }
   } else if (kFp8 && ok && (warp == 2 || warp == 3)) {
@@ -406,9 +456,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int g = 0;
     bool failed = false;
     while (!failed && it.next(pc)) {
+      MaskStream<kSparse> ms;
+      ms.start(p, pc);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const int rs = g % kRawNS, s = g % NS;
-        const uint64_t vmask = tile_mask<kSparse>(p, pc.v, t, pc.len, false);
+        const uint64_t vmask = ms.next(p, t, false);
         if (!warp_ok(wait(bar(C::B_RFULL + rs), (g / kRawNS) & 1, guard)) ||
             !warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) {
           failed = true;
@@ -459,8 +511,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (ok && warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer: issues whichever of QK^T / P.V is ready ----------------
+  } else if (ok && lane == 0 && (warp == 1 || (kSplitIssue && warp == 2))) {
+    // ---------------- UMMA issue ----------------
     // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
     // caches) and of the RoPE QK^T (the cache's RoPE dims: bf16 unless fp16)
     constexpr bool kLatBf16 = !(kFp16 || kFp8);
@@ -471,84 +523,144 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // elements of K), +128 by 2048 B (16 tokens of the MN-major V operand)
     const uint64_t d_p = sdesc_sw128(sb + C::OFF_P, 16, 1024);
     const uint64_t d_qr = sdesc_sw64(sb + C::OFF_QR, 16, 512);
-    PieceIter it(p, part);
-    Piece pc;
-    bool have = it.next(pc);
-    int qk_t = have ? pc.t0 : 0;   // next QK^T tile within the current piece
-    int qk_g = 0, pv_g = 0;        // next global tile for QK^T / P.V
-    int k_piece = 0;               // piece index of qk_g
-    bool q_ready = false;
-    uint32_t first_bits = 0;       // bit (g & 31): tile g is the first of its piece
-    int piece_of[4] = {0, 0, 0, 0};
-    uint64_t t_last = globaltimer();
-    while (true) {
-      bool progressed = false;
-      if (have) {
-        if (!q_ready && mbar_test(bar(C::B_QFULL), k_piece & 1)) q_ready = true;
-        const int s = qk_g % NS, sbuf = qk_g & 1;
-        if (q_ready && mbar_test(bar(C::B_FULL + s), (qk_g / NS) & 1) &&
-            mbar_test(bar(C::B_SEMPTY + sbuf), ((qk_g >> 1) & 1) ^ 1)) {
-          tc_fence_after();
-          const uint32_t dS = tmem + kColS + 64u * sbuf;
-          const uint32_t slot = sb + C::OFF_RING + s * kSlot;
-          const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
-          const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
+    // S[g&1] = Q K^T over this CTA's 256 latent + 32 RoPE dims of tile g
+    auto issue_qk = [&](int g) {
+      const int s = g % NS, sbuf = g & 1;
+      const uint32_t dS = tmem + kColS + 64u * sbuf;
+      const uint32_t slot = sb + C::OFF_RING + s * kSlot;
+      const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
+      const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
 #pragma unroll
-          for (int ci = 0; ci < 4; ++ci) {
+      for (int ci = 0; ci < 4; ++ci) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ts(dS, tmem + kColQ + 32u * ci + 8u * k, d_k + (uint64_t)(ci * (kKChunk >> 4) + 2 * k), idesc_qk,
-                      (ci | k) ? 1u : 0u);
-          }
-          umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
-          umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
-          umma_commit(bar(C::B_SFULL + sbuf));
-          const bool first = qk_t == pc.t0;
-          first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
-          piece_of[qk_g & 3] = k_piece;
-          ++qk_g;
-          if (++qk_t == pc.t1) {
-            umma_commit(bar(C::B_QEMPTY));
-            have = it.next(pc);
-            if (have) qk_t = pc.t0;
-            ++k_piece;
-            q_ready = false;
-          }
-          progressed = true;
-        }
+        for (int k = 0; k < 4; ++k)
+          umma_ts(dS, tmem + kColQ + 32u * ci + 8u * k, d_k + (uint64_t)(ci * (kKChunk >> 4) + 2 * k), idesc_qk,
+                  (ci | k) ? 1u : 0u);
       }
-      if (pv_g < qk_g && mbar_test(bar(C::B_PFULL), pv_g & 1)) {
-        const bool first = (first_bits >> (pv_g & 31)) & 1u;
-        const int pk = piece_of[pv_g & 3];
-        if (!first || pk == 0 || mbar_test(bar(C::B_OEMPTY), (pk - 1) & 1)) {
-          tc_fence_after();
-          const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (pv_g % NS) * kSlot, kKChunk, 1024);
-          umma_ss(tmem, d_p, d_v, idesc_pv, first ? 0u : 1u);
-          umma_ss(tmem, d_p + 2, d_v + 128, idesc_pv, 1u);
-          umma_ss(tmem, d_p + 4, d_v + 256, idesc_pv, 1u);
-          umma_ss(tmem, d_p + 6, d_v + 384, idesc_pv, 1u);
-          umma_commit(bar(C::B_PEMPTY));
-          umma_commit(bar(C::B_EMPTY + pv_g % NS));
-          ++pv_g;
-          progressed = true;
+      umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
+      umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
+      umma_commit(bar(C::B_SFULL + sbuf));
+    };
+    // O[:, this CTA's 256 dims] (+)= P V of tile g; frees P and the ring slot
+    auto issue_pv = [&](int g, bool first) {
+      const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (g % NS) * kSlot, kKChunk, 1024);
+      umma_ss(tmem, d_p, d_v, idesc_pv, first ? 0u : 1u);
+      umma_ss(tmem, d_p + 2, d_v + 128, idesc_pv, 1u);
+      umma_ss(tmem, d_p + 4, d_v + 256, idesc_pv, 1u);
+      umma_ss(tmem, d_p + 6, d_v + 384, idesc_pv, 1u);
+      umma_commit(bar(C::B_PEMPTY));
+      umma_commit(bar(C::B_EMPTY + g % NS));
+    };
+    uint32_t drain_bar = bar(C::B_DRAIN);
+    if constexpr (kSplitIssue) {
+      // Two issuing threads: warp 1 issues QK^T, warp 2 issues P . V, so a
+      // P . V (on the pair's critical path) never queues behind the issue of
+      // a whole QK^T tile. Each waits only on its own inputs.
+      PieceIter it(p, part);
+      Piece pc;
+      int g = 0, k = 0;
+      bool failed = false;
+      if (warp == 1) {
+        while (!failed && it.next(pc)) {
+          if (!wait(bar(C::B_QFULL), k & 1, guard)) break;
+          for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+            if (!wait(bar(C::B_FULL + g % NS), (g / NS) & 1, guard) ||
+                !wait(bar(C::B_SEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1, guard)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(g);
+          }
+          if (failed) break;
+          umma_commit(bar(C::B_QEMPTY));
+          ++k;
         }
-      }
-      if (!have && pv_g == qk_g) break;
-      if (progressed) {
-        t_last = globaltimer();
       } else {
-        if (*abort_flag) break;
-        if (globaltimer() - t_last > guard.limit_ns) {
-          *abort_flag = 1u;
-          atomicOr(p.status, STATUS_TIMEOUT);
-          break;
+        drain_bar = bar(C::B_DRAIN2);
+        while (!failed && it.next(pc)) {
+          for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+            // a piece's first P . V overwrites O: the previous piece's epilogue must have read it
+            if (!wait(bar(C::B_PFULL), g & 1, guard) ||
+                (t == pc.t0 && k > 0 && !wait(bar(C::B_OEMPTY), (k - 1) & 1, guard))) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(g, t == pc.t0);
+          }
+          ++k;
+        }
+      }
+    } else {
+      // One issuing thread that polls its inputs and issues whichever of
+      // QK^T / P . V is ready (the FP8 modes use warps 2-3 for dequantising).
+      PieceIter it(p, part);
+      Piece pc;
+      bool have = it.next(pc);
+      int qk_t = have ? pc.t0 : 0;   // next QK^T tile within the current piece
+      int qk_g = 0, pv_g = 0;        // next global tile for QK^T / P.V
+      int k_piece = 0;               // piece index of qk_g
+      bool q_ready = false;
+      uint32_t first_bits = 0;       // bit (g & 31): tile g is the first of its piece
+      int piece_of[4] = {0, 0, 0, 0};
+      uint64_t t_last = 0;           // start of the current idle stretch (0: none)
+      int idle = 0;
+      while (true) {
+        bool progressed = false;
+        if (have) {
+          if (!q_ready && mbar_test(bar(C::B_QFULL), k_piece & 1)) q_ready = true;
+          if (q_ready && mbar_test(bar(C::B_FULL + qk_g % NS), (qk_g / NS) & 1) &&
+              mbar_test(bar(C::B_SEMPTY + (qk_g & 1)), ((qk_g >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            issue_qk(qk_g);
+            const bool first = qk_t == pc.t0;
+            first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
+            piece_of[qk_g & 3] = k_piece;
+            ++qk_g;
+            if (++qk_t == pc.t1) {
+              umma_commit(bar(C::B_QEMPTY));
+              have = it.next(pc);
+              if (have) qk_t = pc.t0;
+              ++k_piece;
+              q_ready = false;
+            }
+            progressed = true;
+          }
+        }
+        if (pv_g < qk_g && mbar_test(bar(C::B_PFULL), pv_g & 1)) {
+          const bool first = (first_bits >> (pv_g & 31)) & 1u;
+          const int pk = piece_of[pv_g & 3];
+          if (!first || pk == 0 || mbar_test(bar(C::B_OEMPTY), (pk - 1) & 1)) {
+            tc_fence_after();
+            issue_pv(pv_g, first);
+            ++pv_g;
+            progressed = true;
+          }
+        }
+        if (!have && pv_g == qk_g) break;
+        // the wait limit is checked after every 64 idle polls
+        if (progressed) {
+          idle = 0;
+          t_last = 0;
+        } else if (++idle == 64) {
+          idle = 0;
+          if (*abort_flag) break;
+          const uint64_t now = cycles();
+          if (t_last == 0) {
+            t_last = now;
+          } else if (now - t_last > guard.limit) {
+            *abort_flag = 1u;
+            atomicOr(p.status, STATUS_TIMEOUT);
+            break;
+          }
         }
       }
     }
-    // every UMMA issued above has completed before TMEM is released
-    umma_commit(bar(C::B_DRAIN));
-    const uint64_t t_0 = globaltimer();
-    while (!mbar_try_wait(bar(C::B_DRAIN), 0) && globaltimer() - t_0 < 200000000ull) {}
+    // every UMMA this thread issued has completed before TMEM is released
+    umma_commit(drain_bar);
+    const uint64_t t_0 = cycles();
+    while (!mbar_try_wait(drain_bar, 0) && cycles() - t_0 < kDrainLimitCycles) {}
   } else if (ok && warp >= 4 && warp < 8) {
     // ---------------- E warps: S -> E = exp2(x - m_own), stage, send ----------------
     const int h = 32 * (warp - 4) + lane;                 // head = TMEM lane
@@ -591,10 +703,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool failed = false;
     while (!failed && it.next(pc)) {
       if (!load_q(pc, qi++)) break;
-      uint64_t vm_next = tile_mask<kSparse>(p, pc.v, pc.t0, pc.len, rank == 0 && warp == 4);
+      MaskStream<kSparse> ms;
+      ms.start(p, pc);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const uint64_t vm = vm_next;
-        if (t + 1 < pc.t1) vm_next = tile_mask<kSparse>(p, pc.v, t + 1, pc.len, rank == 0 && warp == 4);
+        const uint64_t vm = ms.next(p, t, rank == 0 && warp == 4);
         const int sbuf = g & 1;
         if (!warp_ok(wait(bar(C::B_SFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
         tc_fence_after();
@@ -605,23 +717,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + sbuf));
+        // row max of the raw scores (the scale is positive, so it commutes
+        // with the max); masked tokens become -inf (their rows may hold NaN)
+        if (vm != ~0ull) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (!((vm >> k) & 1ull)) sr[k] = 0xFF800000u;  // -inf
+        }
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
-          const float a = (vm >> k) & 1ull ? __uint_as_float(sr[k]) * sl2 : -INFINITY;
-          const float b2 = (vm >> (k + 1)) & 1ull ? __uint_as_float(sr[k + 1]) * sl2 : -INFINITY;
-          sr[k] = __float_as_uint(a);
-          sr[k + 1] = __float_as_uint(b2);
-          m0 = fmaxf(m0, a);
-          m1 = fmaxf(m1, b2);
+          m0 = fmaxf(m0, __uint_as_float(sr[k]));
+          m1 = fmaxf(m1, __uint_as_float(sr[k + 1]));
         }
-        const float m_own = fmaxf(m0, m1);
-        const float mref = m_own == -INFINITY ? 0.f : m_own;
+        const float m_own = fmaxf(m0, m1) * sl2;
+        const float nref = m_own == -INFINITY ? 0.f : -m_own;
         uint32_t e[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u)
-          e[u] = pack_f16x2(exp2_approx(__uint_as_float(sr[2 * u]) - mref),
-                            exp2_approx(__uint_as_float(sr[2 * u + 1]) - mref));
+          e[u] = pack_f16x2(exp2_approx(fmaf(__uint_as_float(sr[2 * u]), sl2, nref)),
+                            exp2_approx(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nref)));
         // XS[g&1] is free once this CTA's P warps have read tile g-2 from it,
         // and the peer's receive buffer once the peer has read tile g-1
         if (!warp_ok(wait(bar(C::B_XSFREE + sbuf), ((g >> 1) & 1) ^ 1, guard)) ||

@@ -63,6 +63,18 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the latent dims of a 16-bit cache as [rows][9 chunks of 64 dims]: dims {64, rows, 9}, one box = 64 rows x 4 chunks
+bool make_map_chunks(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, 9};
+  cuuint64_t strides[2] = {kDK * 2, 128};
+  cuuint32_t box[3] = {64, 64, 4};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // per-device number of co-resident 2-CTA clusters of the decode kernel
 std::atomic<int> g_parts[kMaxDevices];
 std::once_flag g_attr_once[kMaxDevices];
@@ -219,7 +231,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
         !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B))
       return MLA_ERR_CUDA;
   } else {
-    if (!make_map(&tm_kv, kvcache, dt, 2, kvrows, kDK, kDK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!make_map_chunks(&tm_kv, kvcache, dt, kvrows) ||
         !make_map(&tm_kvr, kvcache, dt, 2, kvrows, kDK, kDK * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
       return MLA_ERR_CUDA;
     tm_sc = tm_kv;

@@ -19,11 +19,17 @@ constexpr uint32_t STATUS_STALE = 4u;    // metadata does not match the call
 // ---------------------------------------------------------------------------
 MLA_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-MLA_DEV uint64_t globaltimer() {
+// SM cycle counter: cheap to read, used for every wait limit (a limit in
+// cycles is a limit in time within the clock range of the part)
+MLA_DEV uint64_t cycles() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
   return t;
 }
+// about two seconds at the top SM clock, longer below it
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;
+// limit of the short waits at tear-down (about 0.2 s)
+constexpr uint64_t kDrainLimitCycles = 400000000ull;
 
 MLA_DEV uint32_t cluster_ctarank() {
   uint32_t r;
@@ -95,19 +101,19 @@ MLA_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
 struct Guard {
   volatile uint32_t* abort;  // in shared memory
   uint32_t* status;          // global status word
-  uint64_t limit_ns;
+  uint64_t limit;            // cycles
 };
 
 template <bool kCluster>
 MLA_DEV bool wait_impl(uint32_t bar, uint32_t parity, const Guard& g) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = cycles();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*g.abort) return false;
-    if (globaltimer() - t0 > g.limit_ns) {
+    if (cycles() - t0 > g.limit) {
       *g.abort = 1u;
       atomicOr(g.status, STATUS_TIMEOUT);
       return false;
@@ -140,11 +146,12 @@ MLA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
-// hint: bring a tensor tile into L2 (no completion tracking)
-MLA_DEV void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y)
-               : "memory");
+MLA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
 }
 // non-blocking test of an mbarrier phase
 MLA_DEV bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -305,6 +312,19 @@ MLA_DEV void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
 // named barrier over `count` threads (id 1..15)
 MLA_DEV void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// named barrier that also returns the OR of `pred` over the participating
+// threads (non-aligned form: the threads of a warp may arrive apart)
+MLA_DEV bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+  return r != 0;
+}
+MLA_DEV void named_sync_na(uint32_t id, uint32_t count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // programmatic dependent launch
