@@ -788,9 +788,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ep[4 * u + 2] = __float_as_uint(o.z); ep[4 * u + 3] = __float_as_uint(o.w);
         }
         const float m_peer = xr_m[h];
-        // loads returned: a relaxed arrive lets the peer overwrite the buffer
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote);
+        {
+          // Hand the receive buffer back to the peer. The arrive is relaxed,
+          // so it must not be performed before this warp's loads from the
+          // buffer have returned: its address depends on every loaded value
+          // (through a mask that is zero at run time, the rank being 0 or 1).
+          uint32_t dep = __float_as_uint(m_peer);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) dep |= ep[4 * u];
+          dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
+          if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
+        }
         // (2) this CTA's own E and m of tile g, staged by the E warps
         if (!warp_ok(wait(bar(C::B_XSFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
         const uint32_t xs_row = sb + C::OFF_XS + sbuf * kXStride + h * 128;
