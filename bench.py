@@ -39,6 +39,11 @@ WORKLOADS = {
                                               causal=True),
     # 656-byte FP8 cache, paged, per-row outlier channels x8
     "fp8_dense_b16_l32768": dict(kind="fp8", batch=16, s_q=1, lens=("fixed", 32768), causal=False),
+    # few heads (h_q=16, fp16, identity block table): the transposed kernel
+    # (only sizes whose cache exceeds the 129 MB L2: the timed loop does not flush it)
+    "fewheads_fp16_h16_b16_l8192": dict(kind="few", batch=16, s_q=1, lens=("fixed", 8192), causal=False, h_q=16),
+    "fewheads_fp16_h16_b16_l65536": dict(kind="few", batch=16, s_q=1, lens=("fixed", 65536), causal=False, h_q=16),
+    "fewheads_fp16_h16_b32_l65536": dict(kind="few", batch=32, s_q=1, lens=("fixed", 65536), causal=False, h_q=16),
     # token-sparse over a 131072-token FP8 cache per request, 5% of the slots -1
     "fp8_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False),
     "fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False),
@@ -154,9 +159,18 @@ def build_case(w, device):
                                       outlier_channels=4, device=device)
         return case, None
     seqlens = workload_seqlens(w)
+    if w["kind"] == "few":
+        case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=w["h_q"], dtype=torch_dtype("float16"),
+                                     causal=w["causal"], seed=0, device=device, shuffle=False)
+        return case, seqlens
     case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device,
                                  outlier_channels=4 if w["kind"] == "fp8" else 0)
     return case, seqlens
+
+
+def torch_dtype(name):
+    import torch
+    return getattr(torch, name)
 
 
 def oracle_rate(case, seqlens, budget_s, max_requests=None):
@@ -177,7 +191,7 @@ def oracle_rate(case, seqlens, budget_s, max_requests=None):
         for i in range(s_q):
             L = seqlens[b] - (s_q - 1 - i if causal else 0)
             oracle.attend(q[i], kv[:max(L, 0)], case.softmax_scale)
-            done_flops += 2.0 * 128 * 1088 * max(L, 0)
+            done_flops += 2.0 * case.h_q * 1088 * max(L, 0)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -198,6 +212,7 @@ def run_ours(args, w, rank, world, device):
     case, seqlens = build_case(w, device)
     kind = w["kind"]
     s_q, causal = w["s_q"], w["causal"]
+    h_q = w.get("h_q", 128)
     is_fp8 = kind in ("fp8", "sparse")
     q = case.q
     bt = sl = idx = None
@@ -216,16 +231,16 @@ def run_ours(args, w, rank, world, device):
             kv = raw.view(case.num_blocks, 64, 1, 656)
         else:
             kv = case.kvcache_paged()
-        flops, algo_bytes, kv_bytes = work_counts(seqlens, s_q, causal, row_bytes=656 if is_fp8 else 1152)
+        flops, algo_bytes, kv_bytes = work_counts(seqlens, s_q, causal, h_q=h_q, row_bytes=656 if is_fp8 else 1152)
         meta_args = dict(causal=causal, is_fp8=is_fp8)
-    out = torch.empty(q.shape[0], s_q, 128, 512, dtype=q.dtype, device=device)
-    lse = torch.empty(q.shape[0], s_q, 128, dtype=torch.float32, device=device)
-    meta, ns = mla.mla_get_metadata(sl, s_q, 128, **meta_args)
+    out = torch.empty(q.shape[0], s_q, h_q, 512, dtype=q.dtype, device=device)
+    lse = torch.empty(q.shape[0], s_q, h_q, dtype=torch.float32, device=device)
+    meta, ns = mla.mla_get_metadata(sl, s_q, h_q, **meta_args)
     stream = torch.cuda.current_stream(device)
     dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8, indices=idx)
 
     def step():
-        m, n = mla.mla_get_metadata(sl, s_q, 128, num_sm_parts=meta.parts, **meta_args)
+        m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
         mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
 
     # correctness gate before timing: device status must be clean
@@ -262,7 +277,7 @@ def run_ours(args, w, rank, world, device):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.roofline_steps)]
     for k in range(args.roofline_steps):
         ev[k][0].record(stream)
-        m, n = mla.mla_get_metadata(sl, s_q, 128, num_sm_parts=meta.parts, **meta_args)
+        m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
         ev[k][1].record(stream)
         mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
         ev[k][2].record(stream)
@@ -293,7 +308,7 @@ def run_ours(args, w, rank, world, device):
             btd = next(it_) if bt is not None else None
             sld = next(it_) if sl is not None else None
             idxd = next(it_) if idx is not None else None
-            m, n = mla.mla_get_metadata(sld, s_q, 128, num_sm_parts=meta.parts, **meta_args)
+            m, n = mla.mla_get_metadata(sld, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
             mla.mla_decode_with_kvcache(dev_in[0], kv, btd, sld, 512, m, n, out=out, lse=lse,
                                         softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8, indices=idxd)
             outh.copy_(out, non_blocking=True)
@@ -367,16 +382,17 @@ def main():
     kv_gbs = world * r["kv_bytes"] / t_step / 1e9
     t_roof = max(r["algo_bytes"] / (hbm_peak * 1e9), r["flops"] / (tc_peak * 1e12))
     bound = "hbm" if r["algo_bytes"] / (hbm_peak * 1e9) >= r["flops"] / (tc_peak * 1e12) else "tensor"
+    kname = "mla_decode_fewheads_kernel" if w["kind"] == "few" else "mla_decode_kernel"
     if bound == "hbm":
         achieved = r["algo_bytes"] / r["t_dec"] / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                "kernel": "mla_decode_kernel", "peak_source": f"{peak_src} hbm_gbs"}
+                "kernel": kname, "peak_source": f"{peak_src} hbm_gbs"}
     else:
         achieved = r["flops"] / r["t_dec"] / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": round(achieved / tc_peak, 4), "traffic": None,
-                "kernel": "mla_decode_kernel", "peak_source": f"{peak_src} bf16_tflops"}
+                "kernel": kname, "peak_source": f"{peak_src} bf16_tflops"}
     cpu = None
     if not args.no_cpu_baseline and world == 1 and w["kind"] == "dense":
         cpu_case = r["case"]
@@ -386,11 +402,12 @@ def main():
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w["kind"] == "dense" else "fp8-e4m3 cache, fp16/bf16 MMA",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"dense": "bf16", "few": "fp16"}.get(w["kind"], "fp8-e4m3 cache, fp16/bf16 MMA"),
         "data": "synthetic",
-        "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": 128, "d_qk": 576,
+        "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": w.get("h_q", 128), "d_qk": 576,
                    "d_v": 512, "page_block": 64, "causal": w["causal"],
-                   "cache": {"dense": "bf16", "fp8": "fp8-656B", "sparse": "fp8-656B"}[w["kind"]],
+                   "cache": {"dense": "bf16", "few": "fp16", "fp8": "fp8-656B", "sparse": "fp8-656B"}[w["kind"]],
                    "seqlens": (f"topk {w['topk']} of {SPARSE_TOKENS} per request, 5% -1" if w["kind"] == "sparse"
                                else f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
                                else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),

@@ -64,10 +64,16 @@ typedef enum { MLA_DTYPE_BF16 = 0, MLA_DTYPE_FP16 = 1 } mla_dtype;
 /* Human-readable name of a status code (static string). */
 MLA_API const char* mla_status_string(int status);
 
-/* Number of work partitions ("SM parts") the decode kernels use on `device`:
- * the number of co-resident 2-CTA clusters of the dense/FP8 decode kernel.
- * Returns a value <= 0 on failure (no device). */
+/* Number of work partitions ("SM parts") the 128-head decode kernels use on
+ * `device`: the number of co-resident 2-CTA clusters of the dense/FP8 decode
+ * kernel. Returns a value <= 0 on failure (no device). */
 MLA_API int mla_num_sm_parts(int device);
+
+/* The same for a given number of query heads: h_q = 128 as above; h_q = 16
+ * (the transposed few-heads kernel, one CTA per part, after the FlashMLA-ETAP
+ * page, §3.1) the number of its co-resident CTAs. Returns a value <= 0 on
+ * failure or for an unsupported h_q. */
+MLA_API int mla_num_sm_parts_for(int device, int h_q);
 
 /* Bytes of the metadata buffer for a decode shape. */
 MLA_API size_t mla_metadata_size(int batch, int s_q, int num_sm_parts);
@@ -87,7 +93,8 @@ MLA_API size_t mla_metadata_size(int batch, int s_q, int num_sm_parts);
  * metadata      (device) mla_metadata_size() bytes, written.
  * num_splits    (device) int32 [batch*s_q + 1], written: exclusive prefix sum
  *               of the number of pieces of each virtual request.
- * h_q must be 128 (16 for the few-heads kernel), h_kv must be 1, page_block 64.
+ * h_q must be 128, or 16 for dense 16-bit caches (the few-heads kernel);
+ * h_kv must be 1, page_block 64.
  * Computed entirely on the device (no host synchronisation). The decode call
  * checks on the device that the metadata matches its own arguments and the
  * current cache_seqlens, and reports MLA_ERR_STALE_METADATA otherwise.
@@ -125,6 +132,10 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * workspace    (device) mla_workspace_size() bytes, 256-B aligned; its status
  *              word must be zeroed once before first use (mla_read_status clears it).
  * A request with no visible token gets out = 0 and lse = -inf.
+ * h_q = 128 with any cache; h_q = 16 with a dense 16-bit cache only: the few
+ * heads fill the MMA's N dimension and the 64 tokens of a tile its M
+ * dimension, the transposed formulation S^T = K Q^T, O^T = V^T P^T of the
+ * FlashMLA-ETAP page (§2.2, §3.2); same results and layouts.
  */
 MLA_API mla_status mla_decode_with_kvcache(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
                                    int page_block, const int32_t* block_table, int max_blocks,

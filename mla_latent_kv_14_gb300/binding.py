@@ -46,6 +46,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mla_status_string.argtypes = [c.c_int]
         lib.mla_num_sm_parts.restype = c.c_int
         lib.mla_num_sm_parts.argtypes = [c.c_int]
+        lib.mla_num_sm_parts_for.restype = c.c_int
+        lib.mla_num_sm_parts_for.argtypes = [c.c_int, c.c_int]
         lib.mla_metadata_size.restype = c.c_size_t
         lib.mla_metadata_size.argtypes = [c.c_int, c.c_int, c.c_int]
         lib.mla_workspace_size.restype = c.c_size_t
@@ -93,10 +95,11 @@ def _check(status: int, where: str):
         raise MLAError(status, where)
 
 
-def mla_num_sm_parts(device=None) -> int:
-    n = load_library().mla_num_sm_parts(_dev(device).index)
+def mla_num_sm_parts(device=None, h_q: int = 128) -> int:
+    """Default number of SM parts of the decode kernel for `h_q` query heads."""
+    n = load_library().mla_num_sm_parts_for(_dev(device).index, h_q)
     if n <= 0:
-        raise MLAError(6, "mla_num_sm_parts")
+        raise MLAError(2 if n < 0 else 6, "mla_num_sm_parts")
     return n
 
 
@@ -121,7 +124,7 @@ def mla_get_metadata(cache_seqlens: Optional[torch.Tensor], s_q: int, h_q: int =
         assert cache_seqlens.dtype == torch.int32 and cache_seqlens.is_contiguous()
     assert batch is not None and device is not None
     device = _dev(device)
-    parts = num_sm_parts or mla_num_sm_parts(device)
+    parts = num_sm_parts or mla_num_sm_parts(device, h_q)
     nbytes = lib.mla_metadata_size(batch, s_q, parts)
     meta = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=device)
     num_splits = torch.empty(batch * s_q + 1, dtype=torch.int32, device=device)

@@ -117,137 +117,7 @@ struct Cfg {
 static_assert(Cfg<MODE_BF16>::kSmemBytes <= 232448, "shared memory");
 static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
-// iteration over the pieces of one SM part (every role walks the same list)
-struct Piece {
-  int v, t0, t1, len, split;
-  bool fin;
-};
-struct PieceIter {
-  const DecodeParams* p;
-  int bv, bt, ev, et, first_split;
-  int v;
-  __device__ __forceinline__ PieceIter(const DecodeParams& prm, int part) : p(&prm) {
-    const int32_t* r = prm.meta + H_WORDS + part * P_WORDS;
-    bv = r[P_BV]; bt = r[P_BT]; ev = r[P_EV]; et = r[P_ET]; first_split = r[P_SPLIT];
-    const int V = prm.batch * prm.s_q;
-    if (bv < 0 || bv >= V || ev < bv || ev >= V) { bv = 0; ev = -1; }  // empty part
-    v = bv - 1;
-  }
-  // advance to the next non-empty piece; false when done
-  __device__ __forceinline__ bool next(Piece& pc) {
-    while (++v <= ev) {
-      int len;
-      const int n = vreq_tiles(p->seqlens, p->topk, p->batch, p->s_q, p->causal, v, &len);
-      int t0 = (v == bv) ? bt : 0;
-      int t1 = (v == ev) ? et : n;
-      t0 = t0 < 0 ? 0 : t0;
-      t1 = t1 > n ? n : t1;
-      if (t1 <= t0) continue;
-      const int ord = (v == bv) ? first_split : 0;
-      const int off = p->split_off[v];
-      const int ns = p->split_off[v + 1] - off;
-      pc.v = v; pc.t0 = t0; pc.t1 = t1; pc.len = len; pc.split = off + ord; pc.fin = (ns == 1);
-      return true;
-    }
-    return false;
-  }
-};
-
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
-
-// Tile validity masks, computed by a whole warp, bit k = token 64t+k.
-// Dense: the first min(len - 64t, 64) tokens, or none if the tile's page is
-// out of range (reported). Sparse: the index-list entries in [0, num_rows);
-// -1 is skipped silently, other out-of-range entries are reported.
-// The global loads behind a mask (block-table entries, index-list entries) are
-// issued well before the mask is needed: a dense stream loads the pages of 32
-// tiles per warp-wide load, one block ahead; a sparse stream loads the indices
-// of tile t+2 while tile t is processed.
-__device__ __forceinline__ int load_pages32(const DecodeParams& p, int b, int t) {
-  const int tt = t + (int)(threadIdx.x & 31);
-  return tt < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + tt) : -1;
-}
-__device__ __forceinline__ uint64_t dense_mask(const DecodeParams& p, int page, int t, int len, bool report) {
-  int nv = len - t * kTile;
-  nv = nv > kTile ? kTile : nv;
-  if (page < 0 || page >= p.num_blocks) {
-    if (report && (threadIdx.x & 31) == 0) atomicOr(p.status, STATUS_INDEX);
-    nv = 0;
-  }
-  return nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
-}
-__device__ __forceinline__ void sparse_fetch(const DecodeParams& p, int v, int t, int& i0, int& i1) {
-  const int b = v % p.batch, i = v / p.batch;
-  const int32_t* row = p.indices + (int64_t)(b * p.s_q + i) * p.topk;
-  const int k = 64 * t + (int)(threadIdx.x & 31);
-  i0 = k < p.topk ? __ldg(row + k) : -1;
-  i1 = k + 32 < p.topk ? __ldg(row + k + 32) : -1;
-}
-__device__ __forceinline__ uint64_t sparse_mask(const DecodeParams& p, int i0, int i1, bool report) {
-  const bool ok0 = i0 >= 0 && (int64_t)i0 < p.num_rows;
-  const bool ok1 = i1 >= 0 && (int64_t)i1 < p.num_rows;
-  const bool bad = (i0 != -1 && !ok0) || (i1 != -1 && !ok1);
-  const uint32_t lo = __ballot_sync(0xffffffffu, ok0), hi = __ballot_sync(0xffffffffu, ok1);
-  if (report && __any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(p.status, STATUS_INDEX);
-  return (uint64_t)lo | ((uint64_t)hi << 32);
-}
-
-// The pages of one dense request seen through a 64-tile window: lane i holds
-// the page of tile base+i (cur) and base+32+i (nxt); moving the window loads
-// the block after next, 32 tiles before it is used.
-struct PageWindow {
-  int b, base, cur, nxt;
-  __device__ __forceinline__ void start(const DecodeParams& p, int b_, int t0) {
-    b = b_;
-    base = t0;
-    cur = load_pages32(p, b, t0);
-    nxt = load_pages32(p, b, t0 + 32);
-  }
-  __device__ __forceinline__ void advance(const DecodeParams& p, int t) {
-    while (t - base >= 32) {
-      base += 32;
-      cur = nxt;
-      nxt = load_pages32(p, b, base + 32);
-    }
-  }
-  // t - base in [0, 64); every lane calls it with the same t
-  __device__ __forceinline__ int get(int t) const {
-    const int d = t - base;
-    const int a = __shfl_sync(0xffffffffu, cur, d & 31);
-    const int c = __shfl_sync(0xffffffffu, nxt, d & 31);
-    return d < 32 ? a : c;
-  }
-};
-
-// masks of consecutive tiles t0, t0+1, ... of one piece (one call per tile)
-template <bool kSparse>
-struct MaskStream {
-  int v, len;
-  PageWindow w;
-  int a0, a1, c0, c1;  // sparse: indices of the next two tiles
-  __device__ __forceinline__ void start(const DecodeParams& p, const Piece& pc) {
-    v = pc.v;
-    len = pc.len;
-    if constexpr (kSparse) {
-      sparse_fetch(p, v, pc.t0, a0, a1);
-      sparse_fetch(p, v, pc.t0 + 1, c0, c1);
-    } else {
-      w.start(p, v % p.batch, pc.t0);
-    }
-  }
-  __device__ __forceinline__ uint64_t next(const DecodeParams& p, int t, bool report) {
-    if constexpr (kSparse) {
-      const uint64_t m = sparse_mask(p, a0, a1, report);
-      a0 = c0;
-      a1 = c1;
-      sparse_fetch(p, v, t + 2, c0, c1);
-      return m;
-    } else {
-      w.advance(p, t);
-      return dense_mask(p, w.get(t), t, len, report);
-    }
-  }
-};
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
   uint32_t r;

@@ -12,6 +12,7 @@
 
 #include "../../include/mla.h"
 #include "decode_dense.cuh"
+#include "decode_fewheads.cuh"
 #include "params.h"
 #include "quant.cuh"
 #include "sched.cuh"
@@ -21,6 +22,7 @@ using namespace mla;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kFewHeads = few::kNH;  // query heads of the transposed few-heads kernel
 
 mla_status cuda_fail(cudaError_t e) {
   (void)cudaGetLastError();
@@ -63,20 +65,25 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// the latent dims of a 16-bit cache as [rows][9 chunks of 64 dims]: dims {64, rows, 9}, one box = 64 rows x 4 chunks
-bool make_map_chunks(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows) {
+// A [rows, 576] 16-bit tensor seen as [rows][9 chunks of 64 dims]: dims {64,
+// rows, 9} with chunk stride 128 B; one box = box_rows rows x box_chunks chunks,
+// laid out in shared memory chunk-major (128-B swizzled 64-dim rows).
+bool make_map_chunks(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows, uint32_t box_rows,
+                     uint32_t box_chunks) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {64, rows, 9};
   cuuint64_t strides[2] = {kDK * 2, 128};
-  cuuint32_t box[3] = {64, 64, 4};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// per-device number of co-resident 2-CTA clusters of the decode kernel
+// per-device number of co-resident 2-CTA clusters of the 128-head decode
+// kernel, and of co-resident CTAs of the few-heads kernel
 std::atomic<int> g_parts[kMaxDevices];
+std::atomic<int> g_parts_few[kMaxDevices];
 std::once_flag g_attr_once[kMaxDevices];
 
 template <typename K>
@@ -96,6 +103,15 @@ cudaError_t prepare_device(int dev) {
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP16>();
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8>();
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8_SPARSE>();
+    if (err == cudaSuccess) err = set_smem(few::mla_decode_fewheads_kernel<false>, few::kSmemBytes);
+    if (err == cudaSuccess) err = set_smem(few::mla_decode_fewheads_kernel<true>, few::kSmemBytes);
+    if (err == cudaSuccess) {
+      int per_sm = 0, sms = 0;
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, few::mla_decode_fewheads_kernel<false>,
+                                                          few::kThreads, few::kSmemBytes);
+      if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (err == cudaSuccess) g_parts_few[dev].store(per_sm * sms > 0 ? per_sm * sms : 1);
+    }
     if (err == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2, 1, 1);
@@ -113,7 +129,8 @@ cudaError_t prepare_device(int dev) {
       if (err == cudaSuccess) g_parts[dev].store(n > 0 ? n : 1);
     }
   });
-  if (err == cudaSuccess && g_parts[dev].load() <= 0) err = cudaErrorInitializationError;
+  if (err == cudaSuccess && (g_parts[dev].load() <= 0 || g_parts_few[dev].load() <= 0))
+    err = cudaErrorInitializationError;
   return err;
 }
 
@@ -145,6 +162,13 @@ int mla_num_sm_parts(int device) {
   return g_parts[device].load();
 }
 
+int mla_num_sm_parts_for(int device, int h_q) {
+  const int n = mla_num_sm_parts(device);
+  if (n <= 0) return n;
+  if (h_q == kFewHeads) return g_parts_few[device].load();
+  return h_q == 128 ? n : -1;
+}
+
 size_t mla_metadata_size(int batch, int s_q, int parts) {
   if (batch <= 0 || s_q <= 0 || parts <= 0) return 0;
   return (size_t)meta_words(batch * s_q, parts) * sizeof(int32_t);
@@ -161,7 +185,8 @@ mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, in
                             void* stream) {
   if (batch <= 0 || s_q <= 0 || parts <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
   if (h_kv != 1 || page_block != kTile) return MLA_ERR_INVALID_ARG;
-  if (h_q != 128) return MLA_ERR_UNSUPPORTED;
+  if (h_q != 128 && h_q != kFewHeads) return MLA_ERR_UNSUPPORTED;
+  if (h_q == kFewHeads && (topk > 0 || is_fp8)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
   if (!metadata || !num_splits) return MLA_ERR_INVALID_ARG;
   if (topk == 0 && !cache_seqlens) return MLA_ERR_INVALID_ARG;
   if (topk > 0 && causal) return MLA_ERR_INVALID_ARG;
@@ -200,7 +225,8 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
   if (num_blocks * (int64_t)page_block >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
-  if (h_q != 128) return MLA_ERR_UNSUPPORTED;
+  if (h_q != 128 && h_q != kFewHeads) return MLA_ERR_UNSUPPORTED;
+  if (h_q == kFewHeads && (indices || is_fp8)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
   if (indices && !is_fp8) return MLA_ERR_UNSUPPORTED;                 // token-sparse decode reads FP8 rows
   if (is_fp8 && q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED; // FP8 rows pair with bf16 queries
   const int64_t qrows = (int64_t)batch * s_q * h_q;
@@ -220,9 +246,19 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   // chunks (128-B swizzle) and 32-dim RoPE halves (64-B swizzle). KV, FP8 rows
   // (bytes): 256 e4m3 per CTA, the 16 scale bytes, 64 RoPE bytes (64-B swizzle).
   CUtensorMap tm_qr, tm_kv, tm_kvr, tm_sc;
-  if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+  const bool few_heads = h_q == kFewHeads;
+  if (few_heads) {
+    // few heads: Q of one query position and a whole 64-token tile, each one
+    // box of all 9 chunks of 64 dims
+    if (!make_map_chunks(&tm_qr, q, dt, (uint64_t)qrows, kFewHeads, 9) ||
+        !make_map_chunks(&tm_kv, kvcache, dt, kvrows, 64, 9))
+      return MLA_ERR_CUDA;
+    tm_kvr = tm_sc = tm_kv;
+  } else if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return MLA_ERR_CUDA;
-  if (mode == dense::MODE_FP8_SPARSE) {
+  }
+  if (few_heads) {
+  } else if (mode == dense::MODE_FP8_SPARSE) {
     tm_kv = tm_kvr = tm_sc = tm_qr;  // rows are fetched by address
   } else if (mode == dense::MODE_FP8) {
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -231,7 +267,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
         !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B))
       return MLA_ERR_CUDA;
   } else {
-    if (!make_map_chunks(&tm_kv, kvcache, dt, kvrows) ||
+    if (!make_map_chunks(&tm_kv, kvcache, dt, kvrows, 64, 4) ||
         !make_map(&tm_kvr, kvcache, dt, 2, kvrows, kDK, kDK * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
       return MLA_ERR_CUDA;
     tm_sc = tm_kv;
@@ -265,7 +301,17 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stages & STAGE_SPLIT) {
+  if ((stages & STAGE_SPLIT) && few_heads) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(parts, 1, 1);
+    cfg.blockDim = dim3(few::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = few::kSmemBytes;
+    cfg.stream = st;
+    if (fp16)
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<true>, tm_qr, tm_kv, p));
+    else
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<false>, tm_qr, tm_kv, p));
+  } else if (stages & STAGE_SPLIT) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * parts, 1, 1);
     cfg.blockDim = dim3(dense::kThreads, 1, 1);
