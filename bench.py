@@ -73,6 +73,24 @@ def workload_seqlens(w):
     return [int(x) for x in synth.uniform_seqlens(w["batch"], w["lens"][1], w["lens"][2], seed=2)]
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of `x` over all ranks (the slowest rank's time);
+    `x` itself on a single process. Works on any process-group backend
+    (NCCL with a CUDA device, gloo with the CPU)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processed
+    `units_per_rank` in at most `seconds` (the max over ranks)."""
+    return world * units_per_rank / seconds
+
+
 def work_counts(seqlens, s_q, causal, h_q=128, row_bytes=1152, indices=None):
     """Algorithmic FLOPs and bytes of one step (no partials, no expansion):
     FLOPs = 2 * h_q * (576 + 512) per visible (query, key) pair; bytes = the
@@ -263,11 +281,8 @@ def run_ours(args, w, rank, world, device):
             step()
         e1.record(stream)
         torch.cuda.synchronize(device)
-    elapsed = e0.elapsed_time(e1) / 1e3
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
     if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
         torch.distributed.barrier()
     st, bits = mla.mla_read_status(device=device)
     if st != 0:
@@ -329,13 +344,10 @@ def run_ours(args, w, rank, world, device):
         t_e2e = max(a0.elapsed_time(a1) / 1e3, 0.0) / n_e2e
         wall = (time.perf_counter() - t0) / n_e2e
         t_e2e = max(t_e2e, wall)
-        if world > 1:
-            t = torch.tensor([t_e2e], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = max_over_ranks(t_e2e, world, device)
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = outh.numel() * outh.element_size() + lseh.numel() * 4
-        e2e = {"value": round(world * flops / t_e2e / 1e12, 3), "unit": "TFLOPS",
+        e2e = {"value": round(whole_job_rate(flops, world, t_e2e) / 1e12, 3), "unit": "TFLOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(t_e2e * 1e3, 4)}
     return dict(elapsed=elapsed, flops=flops, algo_bytes=algo_bytes, kv_bytes=kv_bytes, t_meta=t_meta, t_dec=t_dec,
@@ -378,7 +390,7 @@ def main():
         return
 
     t_step = r["elapsed"] / args.steps
-    tflops = world * r["flops"] / t_step / 1e12
+    tflops = whole_job_rate(r["flops"], world, t_step) / 1e12
     kv_gbs = world * r["kv_bytes"] / t_step / 1e9
     t_roof = max(r["algo_bytes"] / (hbm_peak * 1e9), r["flops"] / (tc_peak * 1e12))
     bound = "hbm" if r["algo_bytes"] / (hbm_peak * 1e9) >= r["flops"] / (tc_peak * 1e12) else "tensor"

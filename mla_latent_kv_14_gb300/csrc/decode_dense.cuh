@@ -647,10 +647,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const int sbuf = g & 1;
-        // (1) the peer's E and m of tile g
+        // (1) this CTA's own E and m of tile g, staged by the E warps (always
+        // before the peer's copy of the same tile lands, so read first)
+        uint32_t ep[32], eo[32];
+        if (!warp_ok(wait(bar(C::B_XSFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
+        const uint32_t xs_row = sb + C::OFF_XS + sbuf * kXStride + h * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 o = ld_shared_v4f(xs_row + ((u ^ (h & 7)) << 4));
+          eo[4 * u] = __float_as_uint(o.x); eo[4 * u + 1] = __float_as_uint(o.y);
+          eo[4 * u + 2] = __float_as_uint(o.z); eo[4 * u + 3] = __float_as_uint(o.w);
+        }
+        const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h];
+        const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_XSFREE + sbuf));
+        float fo[64];  // unpacked while the peer's message is still on its way
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float2 f = unpack_f16x2(eo[u]);
+          fo[2 * u] = f.x;
+          fo[2 * u + 1] = f.y;
+        }
+        // (2) the peer's E and m of tile g
         if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
         if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
-        uint32_t ep[32], eo[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
@@ -669,19 +690,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
           if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
         }
-        // (2) this CTA's own E and m of tile g, staged by the E warps
-        if (!warp_ok(wait(bar(C::B_XSFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
-        const uint32_t xs_row = sb + C::OFF_XS + sbuf * kXStride + h * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 o = ld_shared_v4f(xs_row + ((u ^ (h & 7)) << 4));
-          eo[4 * u] = __float_as_uint(o.x); eo[4 * u + 1] = __float_as_uint(o.y);
-          eo[4 * u + 2] = __float_as_uint(o.z); eo[4 * u + 3] = __float_as_uint(o.w);
-        }
-        const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h];
-        const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_XSFREE + sbuf));
         // (3) P with lazy rescale against the running reference max (P <= 256)
         const float mt = m_own + m_peer;  // upper bound of the tile's scaled row max
         const float m_new = fmaxf(m, mt);
@@ -692,9 +700,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float2 fo = unpack_f16x2(eo[u]), fq = unpack_f16x2(ep[u]);
-          const float a0 = fo.x * fq.x * cf;
-          const float a1 = fo.y * fq.y * cf;
+          const float2 fq = unpack_f16x2(ep[u]);
+          const float a0 = fo[2 * u] * fq.x * cf;
+          const float a1 = fo[2 * u + 1] * fq.y * cf;
           rs0 += a0;
           rs1 += a1;
           ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
