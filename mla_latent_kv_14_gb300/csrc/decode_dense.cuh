@@ -85,9 +85,7 @@ constexpr uint32_t kXStride = 17 * 1024;
 constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
 constexpr uint32_t kRawLat = 64 * 256;     // this CTA's 256 e4m3 per token
-constexpr uint32_t kRawSc = 64 * 16;       // the 4 scales per token
 constexpr uint32_t kRawRope = 64 * 64;     // this CTA's 32 RoPE dims per token (sparse staging)
-constexpr int kRawNS = 2;
 
 // per-mode layout (offsets from a 1024-B aligned base) and barrier indices
 template <int kMode>
@@ -95,7 +93,11 @@ struct Cfg {
   static constexpr bool kFp16 = kMode == MODE_FP16;
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
-  static constexpr int kNS = kFp8 ? 3 : 4;               // KV ring slots (tiles)
+  static constexpr int kNS = kSparse ? 2 : (kFp8 ? 3 : 4);  // KV ring slots (tiles)
+  static constexpr int kRawNS = kSparse ? 3 : 2;          // FP8 raw staging slots
+  // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
+  // them four rows (64 B) at a time into 128-B aligned units
+  static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
   static constexpr uint32_t kRawSlot = kRawLat + kRawSc + (kSparse ? kRawRope : 0);
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
   static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own messages (2 tiles), staged for the copy
@@ -172,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_XEMPTY), kPWarps);  // one arrive per peer P warp
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_DRAIN2), 1);
-    for (int s = 0; s < kRawNS; ++s) {
+    for (int s = 0; s < C::kRawNS; ++s) {
       mbar_init(bar(C::B_RFULL + s), 1);
       mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
     }
@@ -196,11 +198,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------- producer: RoPE dims of Q per piece, KV per tile ----------------
     if (lane == 0) {
       prefetch_tmap(&tm_qr);
-      if constexpr (!kSparse) {
-        prefetch_tmap(&tm_kv);
-        prefetch_tmap(&tm_kvr);
-        if constexpr (kFp8) prefetch_tmap(&tm_sc);
-      }
+      prefetch_tmap(&tm_kv);
+      prefetch_tmap(&tm_kvr);
+      if constexpr (kFp8) prefetch_tmap(&tm_sc);
     }
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
@@ -210,7 +210,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int g = 0, qn = 0;
     int last_g[NS];
     for (int s = 0; s < NS; ++s) last_g[s] = -1;
-    int last_rg[kRawNS] = {-1, -1};
+    int last_rg[C::kRawNS];
+    for (int s = 0; s < C::kRawNS; ++s) last_rg[s] = -1;
     int q_last = -1;
     bool stop = false;
     // block-table entries are loaded one iteration before they are used
@@ -245,10 +246,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pg_next = raw_page(b, t + 1);
           if constexpr (kFp8) {
             // raw e4m3 + scales into the staging ring, converted by the dequant warps
-            const int rs = g % kRawNS;
-            if (!wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
+            const int rs = g % C::kRawNS;
+            if (!wait(bar(C::B_REMPTY + rs), ((g / C::kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
             const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
-            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), kRawLat + kRawSc);
+            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), kRawLat + C::kRawSc);
             tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), 256 * (int)rank, page * kTile, pol_kv);
             tma_load_2d(raw + kRawLat, &tm_sc, bar(C::B_RFULL + rs), 512, page * kTile, pol_kv);
             last_rg[rs] = g;
@@ -266,29 +267,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           last_g[s] = g;
         } else {
-          // sparse: one bulk copy per valid row and field, issued by the whole warp
-          const int rs = g % kRawNS;
-          if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
-          const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
+          // sparse: TMA gather4, four rows per copy; lane j < 16 fetches rows
+          // 4j .. 4j+3 of the tile for each of the three fields (this CTA's
+          // 256 e4m3 bytes, the 16 scale bytes, its 64 RoPE bytes). A row that
+          // is -1 or out of range is fetched as row 0 and masked later.
+          const int rs = g % C::kRawNS;
           const int idx[2] = {n0, n1};
           if (t + 1 < pc.t1) sparse_fetch(p, pc.v, t + 1, n0, n1);  // consumed next tile
-          bool okr[2];
-          int nvalid = 0;
+          if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / C::kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
+          const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
+          const int s0 = (idx[0] >= 0 && (int64_t)idx[0] < p.num_rows) ? idx[0] : 0;
+          const int s1 = (idx[1] >= 0 && (int64_t)idx[1] < p.num_rows) ? idx[1] : 0;
+          int r[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            okr[hh] = idx[hh] >= 0 && (int64_t)idx[hh] < p.num_rows;
-            nvalid += __popc(__ballot_sync(0xffffffffu, okr[hh]));
+          for (int q = 0; q < 4; ++q) {
+            const int row = 4 * (lane & 15) + q;
+            const int a = __shfl_sync(0xffffffffu, s0, row & 31);
+            const int c = __shfl_sync(0xffffffffu, s1, row & 31);
+            r[q] = row < 32 ? a : c;
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), (uint32_t)nvalid * (256 + 16 + 64));
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (256 + 16 + 64));
           __syncwarp();
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            if (!okr[hh]) continue;
-            const int k = 32 * hh + lane;
-            const uint8_t* src = p.kv_fp8 + (int64_t)idx[hh] * kRowBytesFp8;
-            bulk_load(raw + k * 256, src + 256 * rank, 256, bar(C::B_RFULL + rs), pol_kv);
-            bulk_load(raw + kRawLat + k * 16, src + 512, 16, bar(C::B_RFULL + rs), pol_kv);
-            bulk_load(raw + kRawLat + kRawSc + k * 64, src + 528 + 64 * rank, 64, bar(C::B_RFULL + rs), pol_kv);
+          if (lane < 16) {
+            const uint32_t fb = bar(C::B_RFULL + rs);
+            tma_gather4(raw + lane * 4 * 256, &tm_kv, fb, 256 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
+            tma_gather4(raw + kRawLat + lane * 128, &tm_sc, fb, 512, r[0], r[1], r[2], r[3], pol_kv);
+            tma_gather4(raw + kRawLat + C::kRawSc + lane * 4 * 64, &tm_kvr, fb, 528 + 64 * (int)rank, r[0], r[1], r[2],
+                        r[3], pol_kv);
           }
           last_rg[rs] = g;
           // the operand slot is filled by the dequant warps; this arrive only
@@ -306,10 +311,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t t_0 = cycles();
           while (!mbar_try_wait(bar(C::B_FULL + s), (last_g[s] / NS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
         }
-      for (int s = 0; s < kRawNS; ++s)
+      for (int s = 0; s < C::kRawNS; ++s)
         if (last_rg[s] >= 0) {
           const uint64_t t_0 = cycles();
-          while (!mbar_try_wait(bar(C::B_RFULL + s), (last_rg[s] / kRawNS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
+          while (!mbar_try_wait(bar(C::B_RFULL + s), (last_rg[s] / C::kRawNS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
         }
       if (q_last >= 0) {
         const uint64_t t_0 = cycles();
@@ -329,9 +334,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       MaskStream<kSparse> ms;
       ms.start(p, pc);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const int rs = g % kRawNS, s = g % NS;
+        const int rs = g % C::kRawNS, s = g % NS;
         const uint64_t vmask = ms.next(p, t, false);
-        if (!warp_ok(wait(bar(C::B_RFULL + rs), (g / kRawNS) & 1, guard)) ||
+        if (!warp_ok(wait(bar(C::B_RFULL + rs), (g / C::kRawNS) & 1, guard)) ||
             !warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) {
           failed = true;
           break;
@@ -349,7 +354,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if ((vmask >> row) & 1ull) {
             uint32_t lo, hi;
             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 256 + unit * 8));
-            const float sc = scales[row * 4 + 2 * rank + (unit >> 4)];
+            // dense: 16 B per row; sparse: rows 4k..4k+3 share a 128-B unit
+            const int srow = kSparse ? (row >> 2) * 32 + (row & 3) * 4 : row * 4;
+            const float sc = scales[srow + 2 * rank + (unit >> 4)];
             const float2 a = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)));
             const float2 b2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)));
             const float2 c2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)));
@@ -368,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int id = it2 * 64 + tid;
             const int row = id >> 2, u = id & 3;
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if ((vmask >> row) & 1ull) v4 = ld_shared_v4f(raw + kRawLat + kRawSc + row * 64 + u * 16);
+            if ((vmask >> row) & 1ull) v4 = ld_shared_v4f(raw + kRawLat + C::kRawSc + row * 64 + u * 16);
             st_shared_v4(slot + 4 * kKChunk + row * 64 + ((u ^ ((row >> 1) & 3)) << 4), __float_as_uint(v4.x),
                          __float_as_uint(v4.y), __float_as_uint(v4.z), __float_as_uint(v4.w));
           }

@@ -259,7 +259,13 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   }
   if (few_heads) {
   } else if (mode == dense::MODE_FP8_SPARSE) {
-    tm_kv = tm_kvr = tm_sc = tm_qr;  // rows are fetched by address
+    // rows gathered four at a time (TMA gather4: one-row boxes, no swizzle):
+    // this CTA's 256 e4m3 bytes, the 16 scale bytes, its 64 RoPE bytes
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map(&tm_kv, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sc, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 16, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MLA_ERR_CUDA;
   } else if (mode == dense::MODE_FP8) {
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if (!make_map(&tm_kv, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||

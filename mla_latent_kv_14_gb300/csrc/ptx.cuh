@@ -146,6 +146,16 @@ MLA_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
+// Four rows r0..r3 of a 2-D tensor map whose box is one row high, from
+// column x, into four consecutive box rows of shared memory (TMA gather4).
+MLA_DEV void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int r0, int r1, int r2, int r3,
+                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
+      : "memory");
+}
 MLA_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
