@@ -70,10 +70,10 @@ enum : int { MODE_BF16 = 0, MODE_FP16 = 1, MODE_FP8 = 2, MODE_FP8_SPARSE = 3 };
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
 constexpr int kSlot = 4 * kKChunk + kRChunk;
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;              // 16-bit caches (FP8 caches: Cfg::kThreads)
 constexpr int kEWarps = 4;                 // warps 4-7: exponentiate and send
 constexpr int kPWarps = 4;                 // warps 8-11: receive, form P, epilogue
-constexpr int kDequantWarps = 2;           // warps 2-3 (FP8 caches)
+constexpr int kDequantWarps = 4;           // warps 2-3 and 12-13 (FP8 caches)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
 constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
@@ -94,6 +94,7 @@ struct Cfg {
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
   static constexpr int kNS = kSparse ? 2 : (kFp8 ? 3 : 4);  // KV ring slots (tiles)
+  static constexpr int kThreads = kFp8 ? 448 : 384;      // FP8: two more dequant warps (12, 13)
   static constexpr int kRawNS = kSparse ? 3 : 2;          // FP8 raw staging slots
   // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
   // them four rows (64 B) at a time into 128-B aligned units
@@ -128,7 +129,7 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
 }
 
 template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_kv,
                       const __grid_constant__ CUtensorMap tm_kvr, const __grid_constant__ CUtensorMap tm_sc,
                       const DecodeParams p) {
@@ -321,11 +322,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && cycles() - t_0 < kDrainLimitCycles) {}
       }
     }
-  } else if (kFp8 && ok && (warp == 2 || warp == 3)) {
+  } else if (kFp8 && ok && (warp == 2 || warp == 3 || warp >= 12)) {
     // ---------------- dequant: e4m3 x fp32 scale -> fp16 operand tiles ----------------
     // (fp16 keeps 11 bits of the product; the latent QK^T and P.V of FP8
     // caches run as fp16 x fp16, the RoPE QK^T stays bf16 x bf16)
-    const int tid = threadIdx.x - 64;  // 0..63
+    const int tid = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..127 over the four warps
     PieceIter it(p, part);
     Piece pc;
     int g = 0;
@@ -347,8 +348,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 64 rows x 32 units of 8 values; consecutive lanes take consecutive
         // units of one row (conflict-free 8-B loads, 16-B swizzled stores)
 #pragma unroll 4
-        for (int it2 = 0; it2 < 32; ++it2) {
-          const int id = it2 * 64 + tid;
+        for (int it2 = 0; it2 < 16; ++it2) {
+          const int id = it2 * 128 + tid;
           const int row = id >> 5, unit = id & 31;
           uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
           if ((vmask >> row) & 1ull) {
@@ -371,8 +372,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if constexpr (kSparse) {
           // RoPE: staged rows -> 64-byte-swizzled operand chunk
 #pragma unroll
-          for (int it2 = 0; it2 < 4; ++it2) {
-            const int id = it2 * 64 + tid;
+          for (int it2 = 0; it2 < 2; ++it2) {
+            const int id = it2 * 128 + tid;
             const int row = id >> 2, u = id & 3;
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if ((vmask >> row) & 1ull) v4 = ld_shared_v4f(raw + kRawLat + C::kRawSc + row * 64 + u * 16);
@@ -636,7 +637,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (ok && warp >= 8) {
+  } else if (ok && warp >= 8 && warp < 12) {
     // ---------------- P warps: receive, P = E_own * E_peer * 2^(m_own + m_peer - m_ref) ----------------
     const int h = 32 * (warp - 8) + lane;                 // head = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 8)) << 16);

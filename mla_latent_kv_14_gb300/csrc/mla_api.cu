@@ -320,7 +320,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   } else if (stages & STAGE_SPLIT) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * parts, 1, 1);
-    cfg.blockDim = dim3(dense::kThreads, 1, 1);
+    cfg.blockDim = dim3(is_fp8 ? dense::Cfg<dense::MODE_FP8>::kThreads : dense::kThreads, 1, 1);
     cfg.stream = st;
     switch (mode) {
       case dense::MODE_BF16:
