@@ -32,28 +32,31 @@
 // Memory map. TMEM (512 columns): O half [0,256), S buffers [256,320) and
 // [320,384), and this CTA's 256 latent dims of Q as the UMMA A operand
 // [384,512) (column j = bf16 pair (2j, 2j+1) of head row = lane). Shared
-// memory: the peer's message and this CTA's staged message (E_r fp16 128x64 +
-// m_r, 17 KB each), P (bf16, 16 KB), the CTA's 32 RoPE dims of Q (8 KB) and a
-// 4-slot ring of KV tiles (36 KB each: four 64-wide latent chunks, 128-byte
-// swizzled, and one 32-wide RoPE chunk, 64-byte swizzled, of 64 tokens). The
-// producer also prefetches the tiles beyond the ring into L2.
+// memory: the peer's message (E_r fp16 128x64 + m_r + the tile mask, 17 KB),
+// two staged own messages, P (16 KB), the CTA's 32 RoPE dims of Q (8 KB) and a
+// ring of KV tiles (36 KB each: four 64-wide latent chunks, 128-byte swizzled,
+// loaded as one 3-D TMA box, and one 32-wide RoPE chunk, 64-byte swizzled):
+// 4 slots for 16-bit caches, 3 for FP8 caches (whose raw e4m3 rows stage in
+// 2 more slots) and 2 for the sparse mode (3 raw slots, gathered by TMA
+// gather4, four rows per copy).
 //
-// Warp roles (384 threads): warp 0 lane 0 issues TMA loads; warp 1 owns TMEM
-// and lane 0 issues UMMA; warps 4-11 are the softmax / exchange / epilogue
-// warps: warp w serves TMEM lanes (heads) 32*(w%4) .. +31 and the score
-// columns (tokens) [32c, 32c+32) with c = (w-4)/4, so two warps share each
-// head row (the row max is combined through shared memory; the running sums
-// stay per half until the epilogue). They also copy each piece's Q rows into
-// TMEM. Warps 2-3 only take part in set-up and tear-down.
+// Warp roles. Warp 0: producer (TMA; the whole warp in the sparse mode).
+// Warp 1: owns TMEM; lane 0 issues QK^T. Warp kPvWarp (2, or 14 for FP8
+// caches): lane 0 issues P . V, so a P . V never waits behind the issue of a
+// QK^T tile. Warps 2-3 and 12-13 (FP8 caches): e4m3 x scale -> fp16 operand
+// tiles. Warps 4-7 (E): read S, form E_r and the row max, stage them and send
+// them to the peer with one bulk shared-to-shared copy; they also copy each
+// piece's Q rows into TMEM. Warps 8-11 (P): receive the peer's message, form
+// P, rescale O when the running max moves by more than 2^8, and write the
+// piece's output. Warp w of the E and P groups serves TMEM lanes (heads)
+// 32*(w%4) .. +31.
 //
-// Pipeline. A tile's message is one bulk shared-to-shared copy into the peer
-// (the bytes complete on the peer's mbarrier); the buffer-free signal is one
-// remote arrive per warp. The softmax loop runs "receive tile g, exponentiate
-// and send tile g+1, form P of tile g", so each exchange is in flight while the
-// other tile's work runs. The UMMA issuer polls its inputs and issues whichever
-// of QK^T / P.V is ready. Measured on GB300: DSM bulk copies move about 9-18
-// B/clk per SM under load and small single-CTA UMMAs cost 50-70 cycles each to
-// issue; these bound the tile rate.
+// Pipeline. Every hand-off is an mbarrier; every wait is bounded (a wait that
+// gives up sets a status bit and the kernel unwinds). Measured on GB300: a
+// tile's ring slot stays busy from its TMA load through QK^T, the pair
+// exchange (about 1,100 cycles for the 16.5 KB copy), P and P . V, about
+// 9,600 cycles in all, so the tile period is that lifetime over the ring
+// depth; small single-CTA UMMAs cost 50-80 cycles each to issue.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -94,7 +97,9 @@ struct Cfg {
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
   static constexpr int kNS = kSparse ? 2 : (kFp8 ? 3 : 4);  // KV ring slots (tiles)
-  static constexpr int kThreads = kFp8 ? 448 : 384;      // FP8: two more dequant warps (12, 13)
+  // FP8: two more dequant warps (12, 13) and the P . V issuer (14)
+  static constexpr int kThreads = kFp8 ? 480 : 384;
+  static constexpr int kPvWarp = kFp8 ? 14 : 2;          // its lane 0 issues P . V
   static constexpr int kRawNS = kSparse ? 3 : 2;          // FP8 raw staging slots
   // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
   // them four rows (64 B) at a time into 128-B aligned units
@@ -135,7 +140,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
                       const DecodeParams p) {
   using C = Cfg<kMode>;
   constexpr bool kFp16 = C::kFp16, kFp8 = C::kFp8, kSparse = C::kSparse;
-  constexpr bool kSplitIssue = !kFp8;  // warp 2 is free to issue P . V unless it dequantises
   constexpr int NS = C::kNS;
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
@@ -322,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && cycles() - t_0 < kDrainLimitCycles) {}
       }
     }
-  } else if (kFp8 && ok && (warp == 2 || warp == 3 || warp >= 12)) {
+  } else if (kFp8 && ok && (warp == 2 || warp == 3 || warp == 12 || warp == 13)) {
     // ---------------- dequant: e4m3 x fp32 scale -> fp16 operand tiles ----------------
     // (fp16 keeps 11 bits of the product; the latent QK^T and P.V of FP8
     // caches run as fp16 x fp16, the RoPE QK^T stays bf16 x bf16)
@@ -389,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
       }
     }
-  } else if (ok && lane == 0 && (warp == 1 || (kSplitIssue && warp == 2))) {
+  } else if (ok && lane == 0 && (warp == 1 || warp == C::kPvWarp)) {
     // ---------------- UMMA issue ----------------
     // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
     // caches) and of the RoPE QK^T (the cache's RoPE dims: bf16 unless fp16)
@@ -430,109 +434,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       umma_commit(bar(C::B_EMPTY + g % NS));
     };
     uint32_t drain_bar = bar(C::B_DRAIN);
-    if constexpr (kSplitIssue) {
-      // Two issuing threads: warp 1 issues QK^T, warp 2 issues P . V, so a
-      // P . V (on the pair's critical path) never queues behind the issue of
-      // a whole QK^T tile. Each waits only on its own inputs.
-      PieceIter it(p, part);
-      Piece pc;
-      int g = 0, k = 0;
-      bool failed = false;
-      if (warp == 1) {
-        while (!failed && it.next(pc)) {
-          if (!wait(bar(C::B_QFULL), k & 1, guard)) break;
-          for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-            if (!wait(bar(C::B_FULL + g % NS), (g / NS) & 1, guard) ||
-                !wait(bar(C::B_SEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1, guard)) {
-              failed = true;
-              break;
-            }
-            tc_fence_after();
-            issue_qk(g);
-          }
-          if (failed) break;
-          umma_commit(bar(C::B_QEMPTY));
-          ++k;
-        }
-      } else {
-        drain_bar = bar(C::B_DRAIN2);
-        while (!failed && it.next(pc)) {
-          for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-            // a piece's first P . V overwrites O: the previous piece's epilogue must have read it
-            if (!wait(bar(C::B_PFULL), g & 1, guard) ||
-                (t == pc.t0 && k > 0 && !wait(bar(C::B_OEMPTY), (k - 1) & 1, guard))) {
-              failed = true;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(g, t == pc.t0);
-          }
-          ++k;
-        }
-      }
-    } else {
-      // One issuing thread that polls its inputs and issues whichever of
-      // QK^T / P . V is ready (the FP8 modes use warps 2-3 for dequantising).
-      PieceIter it(p, part);
-      Piece pc;
-      bool have = it.next(pc);
-      int qk_t = have ? pc.t0 : 0;   // next QK^T tile within the current piece
-      int qk_g = 0, pv_g = 0;        // next global tile for QK^T / P.V
-      int k_piece = 0;               // piece index of qk_g
-      bool q_ready = false;
-      uint32_t first_bits = 0;       // bit (g & 31): tile g is the first of its piece
-      int piece_of[4] = {0, 0, 0, 0};
-      uint64_t t_last = 0;           // start of the current idle stretch (0: none)
-      int idle = 0;
-      while (true) {
-        bool progressed = false;
-        if (have) {
-          if (!q_ready && mbar_test(bar(C::B_QFULL), k_piece & 1)) q_ready = true;
-          if (q_ready && mbar_test(bar(C::B_FULL + qk_g % NS), (qk_g / NS) & 1) &&
-              mbar_test(bar(C::B_SEMPTY + (qk_g & 1)), ((qk_g >> 1) & 1) ^ 1)) {
-            tc_fence_after();
-            issue_qk(qk_g);
-            const bool first = qk_t == pc.t0;
-            first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
-            piece_of[qk_g & 3] = k_piece;
-            ++qk_g;
-            if (++qk_t == pc.t1) {
-              umma_commit(bar(C::B_QEMPTY));
-              have = it.next(pc);
-              if (have) qk_t = pc.t0;
-              ++k_piece;
-              q_ready = false;
-            }
-            progressed = true;
-          }
-        }
-        if (pv_g < qk_g && mbar_test(bar(C::B_PFULL), pv_g & 1)) {
-          const bool first = (first_bits >> (pv_g & 31)) & 1u;
-          const int pk = piece_of[pv_g & 3];
-          if (!first || pk == 0 || mbar_test(bar(C::B_OEMPTY), (pk - 1) & 1)) {
-            tc_fence_after();
-            issue_pv(pv_g, first);
-            ++pv_g;
-            progressed = true;
-          }
-        }
-        if (!have && pv_g == qk_g) break;
-        // the wait limit is checked after every 64 idle polls
-        if (progressed) {
-          idle = 0;
-          t_last = 0;
-        } else if (++idle == 64) {
-          idle = 0;
-          if (*abort_flag) break;
-          const uint64_t now = cycles();
-          if (t_last == 0) {
-            t_last = now;
-          } else if (now - t_last > guard.limit) {
-            *abort_flag = 1u;
-            atomicOr(p.status, STATUS_TIMEOUT);
+    // Two issuing threads: warp 1 issues QK^T, warp kPvWarp issues P . V, so a
+    // P . V (on the pair's critical path) never queues behind the issue of
+    // a whole QK^T tile. Each waits only on its own inputs.
+    PieceIter it(p, part);
+    Piece pc;
+    int g = 0, k = 0;
+    bool failed = false;
+    if (warp == 1) {
+      while (!failed && it.next(pc)) {
+        if (!wait(bar(C::B_QFULL), k & 1, guard)) break;
+        for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+          if (!wait(bar(C::B_FULL + g % NS), (g / NS) & 1, guard) ||
+              !wait(bar(C::B_SEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1, guard)) {
+            failed = true;
             break;
           }
+          tc_fence_after();
+          issue_qk(g);
         }
+        if (failed) break;
+        umma_commit(bar(C::B_QEMPTY));
+        ++k;
+      }
+    } else {
+      drain_bar = bar(C::B_DRAIN2);
+      while (!failed && it.next(pc)) {
+        for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+          // a piece's first P . V overwrites O: the previous piece's epilogue must have read it
+          if (!wait(bar(C::B_PFULL), g & 1, guard) ||
+              (t == pc.t0 && k > 0 && !wait(bar(C::B_OEMPTY), (k - 1) & 1, guard))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(g, t == pc.t0);
+        }
+        ++k;
       }
     }
     // every UMMA this thread issued has completed before TMEM is released
