@@ -157,7 +157,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
   volatile uint32_t* ok_flag = misc + 2;
   const Guard guard{abort_flag, p.status, kWaitLimitCycles};
 
-  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       // producer (+ the two dequant warps for FP8 caches)
@@ -184,13 +183,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
     }
     *abort_flag = 0u;
-    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
-    if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
-    fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
+  }
+  // Everything above reads no global memory. The schedule, and possibly the
+  // query, cache and tables, come from kernels earlier on the stream; the
+  // launch is a programmatic dependent launch, so wait for them here.
+  pdl_wait();
+  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
+  if (threadIdx.x == 0) {
+    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
+    if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
+    fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();

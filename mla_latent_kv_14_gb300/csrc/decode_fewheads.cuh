@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* ok_flag = misc + 2;
   const Guard guard{abort_flag, p.status, kWaitLimitCycles};
 
-  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(bar(B_FULL + s), 1);
@@ -100,13 +99,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_OEMPTY), kSoftWarps);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0u;
-    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
-    if (!*ok_flag) atomicOr(p.status, STATUS_STALE);
-    fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
+  }
+  // nothing above reads global memory; wait for the kernels this one depends
+  // on (programmatic dependent launch) before the first read
+  pdl_wait();
+  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
+  if (threadIdx.x == 0) {
+    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
+    if (!*ok_flag) atomicOr(p.status, STATUS_STALE);
+    fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();

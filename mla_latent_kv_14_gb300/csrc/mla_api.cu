@@ -307,8 +307,15 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the decode kernels wait for the preceding grid themselves (griddepcontrol),
+  // so they are launched as programmatic dependents of it
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   if ((stages & STAGE_SPLIT) && few_heads) {
     cudaLaunchConfig_t cfg = {};
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     cfg.gridDim = dim3(parts, 1, 1);
     cfg.blockDim = dim3(few::kThreads, 1, 1);
     cfg.dynamicSmemBytes = few::kSmemBytes;
@@ -320,6 +327,8 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   } else if (stages & STAGE_SPLIT) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * parts, 1, 1);
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     cfg.blockDim = dim3(is_fp8 ? dense::Cfg<dense::MODE_FP8>::kThreads : dense::kThreads, 1, 1);
     cfg.stream = st;
     switch (mode) {

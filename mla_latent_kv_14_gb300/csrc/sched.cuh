@@ -100,6 +100,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 //  * a request is cut once per part boundary that falls on one of its tiles
 //    other than its first.
 __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p) {
+  pdl_launch_dependents();  // the decode may start its set-up now; it waits for this grid before reading
   extern __shared__ long long sh[];
   const int V = p.batch * p.s_q;
   long long* C = sh;                                        // [V + 1]
