@@ -73,6 +73,38 @@ def workload_seqlens(w):
     return [int(x) for x in synth.uniform_seqlens(w["batch"], w["lens"][1], w["lens"][2], seed=2)]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def kernel_source_digest() -> str:
+    """Digest of the CUDA sources the kernels are built from (so a stored
+    DRAM-traffic figure is used only for the kernels it was measured on)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "mla_latent_kv_14_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the dominant kernel from one
+    ncu capture, as recorded in profiles/dram_traffic.txt, or None when there
+    is no record for this workload or the kernels changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    digest = kernel_source_digest()
+    for parts in lines:
+        if len(parts) >= 3 and parts[0] == workload and parts[2] == digest:
+            return int(parts[1])
+    return None
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest value of `x` over all ranks (the slowest rank's time);
     `x` itself on a single process. Works on any process-group backend
@@ -410,12 +442,12 @@ def main():
     if bound == "hbm":
         achieved = r["algo_bytes"] / r["t_dec"] / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "frac": round(achieved / hbm_peak, 4), "traffic": stored_traffic(args.workload),
                 "kernel": kname, "peak_source": f"{peak_src} hbm_gbs"}
     else:
         achieved = r["flops"] / r["t_dec"] / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(achieved / tc_peak, 4), "traffic": None,
+                "frac": round(achieved / tc_peak, 4), "traffic": stored_traffic(args.workload),
                 "kernel": kname, "peak_source": f"{peak_src} bf16_tflops"}
     cpu = None
     if not args.no_cpu_baseline and world == 1 and w["kind"] == "dense":
