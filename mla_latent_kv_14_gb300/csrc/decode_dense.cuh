@@ -78,7 +78,8 @@ constexpr int kEWarps = 4;                 // warps 4-7: exponentiate and send
 constexpr int kPWarps = 4;                 // warps 8-11: receive, form P, epilogue
 constexpr int kDequantWarps = 4;           // warps 2-3 and 12-13 (FP8 caches)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;            // S buffers at columns 256 and 320
+constexpr uint32_t kColS = 256;            // S at columns 256..319 (one buffer)
+constexpr uint32_t kColP = 320;            // P of tile g: 16-bit pairs at columns 320 + 32*(g&1)
 constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 384..511
 constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
 constexpr uint32_t kXM = kXE;                           // + m_r per row (fp32)
@@ -96,7 +97,7 @@ struct Cfg {
   static constexpr bool kFp16 = kMode == MODE_FP16;
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
-  static constexpr int kNS = kSparse ? 2 : (kFp8 ? 3 : 4);  // KV ring slots (tiles)
+  static constexpr int kNS = kSparse ? 3 : (kFp8 ? 4 : 5);  // KV ring slots (tiles)
   // FP8: two more dequant warps (12, 13) and the P . V issuer (14)
   static constexpr int kThreads = kFp8 ? 480 : 384;
   static constexpr int kPvWarp = kFp8 ? 14 : 2;          // its lane 0 issues P . V
@@ -106,17 +107,16 @@ struct Cfg {
   static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
   static constexpr uint32_t kRawSlot = kRawLat + kRawSc + (kSparse ? kRawRope : 0);
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
-  static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own messages (2 tiles), staged for the copy
-  static constexpr uint32_t OFF_P = OFF_XS + 2 * kXStride;  // 128 rows x 64 bf16
-  static constexpr uint32_t OFF_QR = OFF_P + 128 * 128;  // 32 RoPE dims of Q: 128 rows x 64 B
+  static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
+  static constexpr uint32_t OFF_QR = OFF_XS + kXStride;  // 32 RoPE dims of Q: 128 rows x 64 B
   static constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
   static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlot;
   static constexpr uint32_t OFF_BAR = OFF_RAW + (kFp8 ? kRawNS * kRawSlot : 0);
   static constexpr uint32_t B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1,
-                            B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2,
-                            B_PEMPTY = B_PFULL + 1, B_OEMPTY = B_PEMPTY + 1, B_XFULL = B_OEMPTY + 1,
+                            B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SEMPTY + 1,
+                            B_PEMPTY = B_PFULL + 2, B_OEMPTY = B_PEMPTY + 2, B_XFULL = B_OEMPTY + 1,
                             B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_XSFREE = B_DRAIN + 1,
-                            B_XSFULL = B_XSFREE + 2, B_RFULL = B_XSFULL + 2,
+                            B_XSFULL = B_XSFREE + 1, B_RFULL = B_XSFULL + 1,
                             B_REMPTY = B_RFULL + kRawNS, B_DRAIN2 = B_REMPTY + kRawNS,
                             B_COUNT = B_DRAIN2 + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem slot, abort flag, ok flag
@@ -165,14 +165,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     }
     mbar_init(bar(C::B_QFULL), kEWarps + 1);  // E warps (latent into TMEM) + RoPE TMA
     mbar_init(bar(C::B_QEMPTY), 1);
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_SEMPTY), kEWarps);
+    mbar_init(bar(C::B_XSFREE), kPWarps);  // P warps have read XS
+    mbar_init(bar(C::B_XSFULL), 1);        // E warps have staged XS
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_SEMPTY + s), kEWarps);
-      mbar_init(bar(C::B_XSFREE + s), kPWarps);  // P warps have read XS[s]
-      mbar_init(bar(C::B_XSFULL + s), 1);        // E warps have staged XS[s]
+      mbar_init(bar(C::B_PFULL + s), kPWarps);  // P of tile g (g&1 = s) is in TMEM
+      mbar_init(bar(C::B_PEMPTY + s), 1);       // its P . V is done
     }
-    mbar_init(bar(C::B_PFULL), kPWarps);
-    mbar_init(bar(C::B_PEMPTY), 1);
     mbar_init(bar(C::B_OEMPTY), kPWarps);
     mbar_init(bar(C::B_XFULL), 1);              // own expect_tx + the peer's copied bytes
     mbar_init(bar(C::B_XEMPTY), kPWarps);  // one arrive per peer P warp
@@ -409,12 +409,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     constexpr uint32_t idesc_pv = idesc_f16(128, 256, kLatBf16, false, true);
     // descriptors: +2 in the low word advances the start address by 32 B (16
     // elements of K), +128 by 2048 B (16 tokens of the MN-major V operand)
-    const uint64_t d_p = sdesc_sw128(sb + C::OFF_P, 16, 1024);
     const uint64_t d_qr = sdesc_sw64(sb + C::OFF_QR, 16, 512);
     // S[g&1] = Q K^T over this CTA's 256 latent + 32 RoPE dims of tile g
     auto issue_qk = [&](int g) {
-      const int s = g % NS, sbuf = g & 1;
-      const uint32_t dS = tmem + kColS + 64u * sbuf;
+      const int s = g % NS;
+      const uint32_t dS = tmem + kColS;
       const uint32_t slot = sb + C::OFF_RING + s * kSlot;
       const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
       const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
@@ -427,16 +426,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       }
       umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
       umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
-      umma_commit(bar(C::B_SFULL + sbuf));
+      umma_commit(bar(C::B_SFULL));
     };
     // O[:, this CTA's 256 dims] (+)= P V of tile g; frees P and the ring slot
     auto issue_pv = [&](int g, bool first) {
       const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (g % NS) * kSlot, kKChunk, 1024);
-      umma_ss(tmem, d_p, d_v, idesc_pv, first ? 0u : 1u);
-      umma_ss(tmem, d_p + 2, d_v + 128, idesc_pv, 1u);
-      umma_ss(tmem, d_p + 4, d_v + 256, idesc_pv, 1u);
-      umma_ss(tmem, d_p + 6, d_v + 384, idesc_pv, 1u);
-      umma_commit(bar(C::B_PEMPTY));
+      const uint32_t tp = tmem + kColP + 32u * (uint32_t)(g & 1);  // P as the A operand, from TMEM
+      umma_ts(tmem, tp, d_v, idesc_pv, first ? 0u : 1u);
+      umma_ts(tmem, tp + 8u, d_v + 128, idesc_pv, 1u);
+      umma_ts(tmem, tp + 16u, d_v + 256, idesc_pv, 1u);
+      umma_ts(tmem, tp + 24u, d_v + 384, idesc_pv, 1u);
+      umma_commit(bar(C::B_PEMPTY + (g & 1)));
       umma_commit(bar(C::B_EMPTY + g % NS));
     };
     uint32_t drain_bar = bar(C::B_DRAIN);
@@ -452,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         if (!wait(bar(C::B_QFULL), k & 1, guard)) break;
         for (int t = pc.t0; t < pc.t1; ++t, ++g) {
           if (!wait(bar(C::B_FULL + g % NS), (g / NS) & 1, guard) ||
-              !wait(bar(C::B_SEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1, guard)) {
+              !wait(bar(C::B_SEMPTY), (g & 1) ^ 1, guard)) {
             failed = true;
             break;
           }
@@ -468,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       while (!failed && it.next(pc)) {
         for (int t = pc.t0; t < pc.t1; ++t, ++g) {
           // a piece's first P . V overwrites O: the previous piece's epilogue must have read it
-          if (!wait(bar(C::B_PFULL), g & 1, guard) ||
+          if (!wait(bar(C::B_PFULL + (g & 1)), (g >> 1) & 1, guard) ||
               (t == pc.t0 && k > 0 && !wait(bar(C::B_OEMPTY), (k - 1) & 1, guard))) {
             failed = true;
             break;
@@ -529,16 +529,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       ms.start(p, pc);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const uint64_t vm = ms.next(p, t, rank == 0 && warp == 4);
-        const int sbuf = g & 1;
-        if (!warp_ok(wait(bar(C::B_SFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
+        if (!warp_ok(wait(bar(C::B_SFULL), g & 1, guard))) { failed = true; break; }
         tc_fence_after();
         uint32_t sr[64];
-        tmem_ld32(tl + kColS + 64u * sbuf, sr);
-        tmem_ld32(tl + kColS + 64u * sbuf + 32u, sr + 32);
+        tmem_ld32(tl + kColS, sr);
+        tmem_ld32(tl + kColS + 32u, sr + 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_SEMPTY + sbuf));
+        if (lane == 0) mbar_arrive(bar(C::B_SEMPTY));
         // row max of the raw scores (the scale is positive, so it commutes
         // with the max); masked tokens become -inf (their rows may hold NaN)
         if (vm != ~0ull) {
@@ -559,25 +558,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         for (int u = 0; u < 32; ++u)
           e[u] = pack_f16x2(exp2_approx(fmaf(__uint_as_float(sr[2 * u]), sl2, nref)),
                             exp2_approx(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nref)));
-        // XS[g&1] is free once this CTA's P warps have read tile g-2 from it,
-        // and the peer's receive buffer once the peer has read tile g-1
-        if (!warp_ok(wait(bar(C::B_XSFREE + sbuf), ((g >> 1) & 1) ^ 1, guard)) ||
+        // XS is free once this CTA's P warps have read tile g-1 from it and the
+        // peer has read its copy (which frees the peer's receive buffer too)
+        if (!warp_ok(wait(bar(C::B_XSFREE), (g & 1) ^ 1, guard)) ||
             !warp_ok(wait_cluster(bar(C::B_XEMPTY), (g & 1) ^ 1, guard))) {
           failed = true;
           break;
         }
-        const uint32_t xs = sb + C::OFF_XS + sbuf * kXStride;
+        const uint32_t xs = sb + C::OFF_XS;
         const uint32_t xs_row = xs + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           st_shared_v4(xs_row + ((u ^ (h & 7)) << 4), e[4 * u], e[4 * u + 1], e[4 * u + 2], e[4 * u + 3]);
-        reinterpret_cast<float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h] = m_own;
-        if (h == 0) *reinterpret_cast<uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask) = vm;
+        reinterpret_cast<float*>(smem + C::OFF_XS + kXM)[h] = m_own;
+        if (h == 0) *reinterpret_cast<uint64_t*>(smem + C::OFF_XS + kXMask) = vm;
         fence_proxy_async_smem();
         named_sync(kEBar, 128);
         if (h == 0) {
           bulk_copy_to_peer(xr_remote, xs, kXBytes, xfull_remote);
-          mbar_arrive(bar(C::B_XSFULL + sbuf));
+          mbar_arrive(bar(C::B_XSFULL));
         }
       }
     }
@@ -587,7 +586,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp - 8)) << 16);
     const uint32_t xr_row = sb + C::OFF_XR + h * 128;
     const uint32_t xempty_remote = mapa(bar(C::B_XEMPTY), peer);
-    const uint32_t p_row = sb + C::OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
     const float* xr_m = reinterpret_cast<const float*>(smem + C::OFF_XR + kXM);
     const int pid = threadIdx.x - 256;                    // 0..127 among P threads
     PieceIter it(p, part);
@@ -598,22 +596,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       float m = -INFINITY, l = 0.f;
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const int sbuf = g & 1;
         // (1) this CTA's own E and m of tile g, staged by the E warps (always
         // before the peer's copy of the same tile lands, so read first)
         uint32_t ep[32], eo[32];
-        if (!warp_ok(wait(bar(C::B_XSFULL + sbuf), (g >> 1) & 1, guard))) { failed = true; break; }
-        const uint32_t xs_row = sb + C::OFF_XS + sbuf * kXStride + h * 128;
+        if (!warp_ok(wait(bar(C::B_XSFULL), g & 1, guard))) { failed = true; break; }
+        const uint32_t xs_row = sb + C::OFF_XS + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 o = ld_shared_v4f(xs_row + ((u ^ (h & 7)) << 4));
           eo[4 * u] = __float_as_uint(o.x); eo[4 * u + 1] = __float_as_uint(o.y);
           eo[4 * u + 2] = __float_as_uint(o.z); eo[4 * u + 3] = __float_as_uint(o.w);
         }
-        const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + sbuf * kXStride + kXM)[h];
-        const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + sbuf * kXStride + kXMask);
+        const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + kXM)[h];
+        const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + kXMask);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_XSFREE + sbuf));
+        if (lane == 0) mbar_arrive(bar(C::B_XSFREE));
         float fo[64];  // unpacked while the peer's message is still on its way
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
@@ -661,10 +658,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
         l = l * alpha + (rs0 + rs1);
         m = m_use;
-        // the previous P . V has finished: P buffer and O are free
-        if (g > 0 && !warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
-        tc_fence_after();
+        // a rescale of O needs every earlier P . V done; they complete in issue
+        // order, so waiting for tile g-1 is enough
         if (__any_sync(0xffffffffu, resc) && t != pc.t0) {
+          if (!warp_ok(wait(bar(C::B_PEMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1, guard))) { failed = true; break; }
+          tc_fence_after();
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             uint32_t r[32];
@@ -685,18 +683,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             if (!((vm >> row) & 1ull))
               st_shared_v4(slot + (u >> 3) * kKChunk + row * 128 + (u & 7) * 16, 0u, 0u, 0u, 0u);
           }
+          fence_proxy_async_smem();
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(p_row + ((u ^ (h & 7)) << 4), ep[4 * u], ep[4 * u + 1], ep[4 * u + 2], ep[4 * u + 3]);
-        fence_proxy_async_smem();
+        // P of tile g into TMEM buffer g&1 (the A operand of P . V), once P . V
+        // of tile g-2 is done with that buffer
+        if (!warp_ok(wait(bar(C::B_PEMPTY + (g & 1)), ((g >> 1) & 1) ^ 1, guard))) { failed = true; break; }
+        tc_fence_after();
+        tmem_st32(tl + kColP + 32u * (uint32_t)(g & 1), ep);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PFULL));
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL + (g & 1)));
       }
       if (failed) break;
       // ---- epilogue of the piece: O / l -> out (single piece) or partial ----
-      if (!warp_ok(wait(bar(C::B_PEMPTY), (g - 1) & 1, guard))) { failed = true; break; }
+      // (P . V of the piece's last tile completes after every earlier one)
+      if (!warp_ok(wait(bar(C::B_PEMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1, guard))) { failed = true; break; }
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
