@@ -155,6 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
   volatile uint32_t* tmem_slot = misc + 0;
   volatile uint32_t* abort_flag = misc + 1;
   volatile uint32_t* ok_flag = misc + 2;
+  volatile uint32_t* qk_started = misc + 3;  // QK^T tiles whose issue has begun
   const Guard guard{abort_flag, p.status, kWaitLimitCycles};
 
   if (threadIdx.x == 0) {
@@ -183,6 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
     }
     *abort_flag = 0u;
+    *qk_started = 0u;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), kTmemCols);
@@ -457,6 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             break;
           }
           tc_fence_after();
+          *qk_started = (uint32_t)g + 1u;
           issue_qk(g);
         }
         if (failed) break;
@@ -472,6 +475,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
               (t == pc.t0 && k > 0 && !wait(bar(C::B_OEMPTY), (k - 1) & 1, guard))) {
             failed = true;
             break;
+          }
+          // The tensor pipe runs MMAs in issue order, and S of the QK^T in
+          // flight is on the loop QK^T -> E reads S -> next QK^T. So P . V
+          // waits for that S to complete and fills the gap while the E warps
+          // read it. S(n-1) is complete once its phase is seen or once QK^T n
+          // has started (it waits for S(n-1) to be read); the wait is
+          // bounded, and giving up only changes the order of the MMAs.
+          const uint32_t n = *qk_started;
+          if (n > 0u) {
+            const uint64_t t_0 = cycles();
+            while (!mbar_test(bar(C::B_SFULL), (n - 1u) & 1u) && *qk_started == n && cycles() - t_0 < 20000u) {}
           }
           tc_fence_after();
           issue_pv(g, t == pc.t0);
@@ -703,31 +717,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
       const int64_t row = (int64_t)(b * p.s_q + i) * 128 + h;
-#pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tl + 32u * cc, r);
-        tmem_wait_ld();
+      // each thread writes 32 consecutive values of its own row per chunk;
+      // 32-byte stores make every request of a warp a whole sector, and the
+      // TMEM load of chunk cc+1 is in flight while chunk cc is stored
+      auto store_chunk = [&](int cc, uint32_t* r) {
         if (pc.fin) {
           OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + 32 * cc;
+          uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 32; k += 8) {
-            uint4 w;
-            const float* f = reinterpret_cast<const float*>(r + k);
-            w.x = kFp16 ? pack_f16x2(f[0] * inv_l, f[1] * inv_l) : pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
-            w.y = kFp16 ? pack_f16x2(f[2] * inv_l, f[3] * inv_l) : pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
-            w.z = kFp16 ? pack_f16x2(f[4] * inv_l, f[5] * inv_l) : pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
-            w.w = kFp16 ? pack_f16x2(f[6] * inv_l, f[7] * inv_l) : pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
-            *reinterpret_cast<uint4*>(dst + k) = w;
+          for (int k = 0; k < 16; ++k) {
+            const float a = __uint_as_float(r[2 * k]) * inv_l, c = __uint_as_float(r[2 * k + 1]) * inv_l;
+            w[k] = kFp16 ? pack_f16x2(a, c) : pack_bf16x2(a, c);
+          }
+          if (p.out_v8) {
+            st_global_v8(dst, w);
+            st_global_v8(dst + 16, w + 8);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)
+              *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(w[k], w[k + 1], w[k + 2], w[k + 3]);
           }
         } else {
           float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * cc;
 #pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(dst + k) =
-                make_float4(__uint_as_float(r[k]) * inv_l, __uint_as_float(r[k + 1]) * inv_l,
-                            __uint_as_float(r[k + 2]) * inv_l, __uint_as_float(r[k + 3]) * inv_l);
+          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * inv_l);
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) st_global_v8(dst + k, r + k);
         }
+      };
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tl, ra);
+      tmem_wait_ld();
+      pin_regs32(ra);
+#pragma unroll 1
+      for (int cc = 0; cc < 8; cc += 2) {
+        tmem_ld32(tl + 32u * (cc + 1), rb);
+        store_chunk(cc, ra);
+        tmem_wait_ld();
+        pin_regs32(rb);
+        if (cc + 2 < 8) tmem_ld32(tl + 32u * (cc + 2), ra);
+        store_chunk(cc + 1, rb);
+        tmem_wait_ld();
+        pin_regs32(ra);
       }
       if (rank == 0) {
         if (pc.fin) p.lse[row] = lse;

@@ -290,6 +290,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.meta = static_cast<const int32_t*>(metadata);
   p.split_off = num_splits;
   p.out = out;
+  p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.lse = lse;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.o_part = reinterpret_cast<float*>(ws + kWsHeader);

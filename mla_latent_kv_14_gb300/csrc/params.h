@@ -64,6 +64,7 @@ struct DecodeParams {
   int64_t num_rows;            // num_blocks * page_block
   int max_blocks;
   int batch, s_q, h_q, topk, causal, is_fp8, parts;
+  int out_v8;                  // out is 32-B aligned: 32-byte stores in the epilogue
   float scale_log2;            // softmax_scale * log2(e)
 };
 

@@ -287,6 +287,11 @@ MLA_DEV void tmem_st32x4(uint32_t taddr, const uint32_t* r) {
   for (int c = 0; c < 4; ++c) tmem_st32(taddr + 32u * c, r + 32 * c);
 }
 MLA_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// keep uses of registers filled by an asynchronous tcgen05.ld after the wait
+MLA_DEV void pin_regs32(uint32_t* r) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) asm volatile("" : "+r"(r[k]));
+}
 MLA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16; A is M x K with row m in lane m and
@@ -316,6 +321,13 @@ MLA_DEV void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
 }
 MLA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// 32-byte global store (dst 32-B aligned): a warp's store of 32 rows fills
+// whole sectors
+MLA_DEV void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 MLA_DEV float4 ld_shared_v4f(uint32_t addr) {
   float4 v;
