@@ -97,11 +97,11 @@ struct Cfg {
   static constexpr bool kFp16 = kMode == MODE_FP16;
   static constexpr bool kFp8 = kMode >= MODE_FP8;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
-  static constexpr int kNS = kSparse ? 3 : (kFp8 ? 4 : 5);  // KV ring slots (tiles)
+  static constexpr int kNS = kSparse ? 3 : (kFp8 ? 3 : 5);  // KV ring slots (tiles)
   // FP8: two more dequant warps (12, 13) and the P . V issuer (14)
   static constexpr int kThreads = kFp8 ? 480 : 384;
   static constexpr int kPvWarp = kFp8 ? 14 : 2;          // its lane 0 issues P . V
-  static constexpr int kRawNS = kSparse ? 3 : 2;          // FP8 raw staging slots
+  static constexpr int kRawNS = 3;                        // FP8 raw staging slots
   // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
   // them four rows (64 B) at a time into 128-B aligned units
   static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
@@ -127,6 +127,11 @@ static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
 
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
@@ -370,14 +375,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             // dense: 16 B per row; sparse: rows 4k..4k+3 share a 128-B unit
             const int srow = kSparse ? (row >> 2) * 32 + (row & 3) * 4 : row * 4;
             const float sc = scales[srow + 2 * rank + (unit >> 4)];
-            const float2 a = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)));
-            const float2 b2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)));
-            const float2 c2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)));
-            const float2 d2 = unpack_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)));
-            w0 = pack_f16x2_sat(a.x * sc, a.y * sc);
-            w1 = pack_f16x2_sat(b2.x * sc, b2.y * sc);
-            w2 = pack_f16x2_sat(c2.x * sc, c2.y * sc);
-            w3 = pack_f16x2_sat(d2.x * sc, d2.y * sc);
+            // e4m3 -> f16 is exact; the product rounds once more through the
+            // fp16 copy of the scale (both roundings are below 2^-11 relative)
+            const uint32_t sc2 = pack_f16x2(sc, sc);
+            w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)), sc2);
+            w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)), sc2);
+            w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)), sc2);
+            w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)), sc2);
           }
           st_shared_v4(slot + (unit >> 3) * kKChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
         }
@@ -625,12 +629,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + kXMask);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_XSFREE));
-        float fo[64];  // unpacked while the peer's message is still on its way
+        // 16-bit caches: unpacked while the peer's message is still on its
+        // way; FP8 caches (128 registers a thread) unpack it as it is used
+        float fo[kFp8 ? 1 : 64];
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float2 f = unpack_f16x2(eo[u]);
-          fo[2 * u] = f.x;
-          fo[2 * u + 1] = f.y;
+          for (int u = 0; u < 32; ++u) {
+            const float2 f = unpack_f16x2(eo[u]);
+            fo[2 * u] = f.x;
+            fo[2 * u + 1] = f.y;
+          }
         }
         // (2) the peer's E and m of tile g
         if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
@@ -664,8 +672,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const float2 fq = unpack_f16x2(ep[u]);
-          const float a0 = fo[2 * u] * fq.x * cf;
-          const float a1 = fo[2 * u + 1] * fq.y * cf;
+          const float2 fw = kFp8 ? unpack_f16x2(eo[u]) : make_float2(fo[(2 * u) % (kFp8 ? 1 : 64)],
+                                                                       fo[(2 * u + 1) % (kFp8 ? 1 : 64)]);
+          const float a0 = fw.x * fq.x * cf;
+          const float a1 = fw.y * fq.y * cf;
           rs0 += a0;
           rs1 += a1;
           ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
