@@ -89,7 +89,6 @@ constexpr uint32_t kXStride = 17 * 1024;
 constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
 constexpr uint32_t kRawLat = 64 * 256;     // this CTA's 256 e4m3 per token
-constexpr uint32_t kRawRope = 64 * 64;     // this CTA's 32 RoPE dims per token (sparse staging)
 
 // per-mode layout (offsets from a 1024-B aligned base) and barrier indices
 template <int kMode>
@@ -105,7 +104,7 @@ struct Cfg {
   // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
   // them four rows (64 B) at a time into 128-B aligned units
   static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
-  static constexpr uint32_t kRawSlot = kRawLat + kRawSc + (kSparse ? kRawRope : 0);
+  static constexpr uint32_t kRawSlot = kRawLat + kRawSc;
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
   static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
   static constexpr uint32_t OFF_QR = OFF_XS + kXStride;  // 32 RoPE dims of Q: 128 rows x 64 B
@@ -304,20 +303,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             const int c = __shfl_sync(0xffffffffu, s1, row & 31);
             r[q] = row < 32 ? a : c;
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (256 + 16 + 64));
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (256 + 16));
           __syncwarp();
           if (lane < 16) {
             const uint32_t fb = bar(C::B_RFULL + rs);
             tma_gather4(raw + lane * 4 * 256, &tm_kv, fb, 256 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
             tma_gather4(raw + kRawLat + lane * 128, &tm_sc, fb, 512, r[0], r[1], r[2], r[3], pol_kv);
-            tma_gather4(raw + kRawLat + C::kRawSc + lane * 4 * 64, &tm_kvr, fb, 528 + 64 * (int)rank, r[0], r[1], r[2],
-                        r[3], pol_kv);
           }
           last_rg[rs] = g;
-          // the operand slot is filled by the dequant warps; this arrive only
-          // completes the producer's share of the barrier
+          // the RoPE dims (bf16 in the row) go straight into the operand slot,
+          // four rows per copy, 64-byte swizzled by the copy; the dequant
+          // warps fill the latent part
           if (!warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) { stop = true; break; }
-          if (lane == 0) mbar_arrive(bar(C::B_FULL + s));
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_FULL + s), 64u * 64u);
+          __syncwarp();
+          if (lane < 16)
+            tma_gather4(sb + C::OFF_RING + s * kSlot + 4 * kKChunk + lane * 4 * 64, &tm_kvr, bar(C::B_FULL + s),
+                        528 + 64 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
           last_g[s] = g;
         }
       }
@@ -384,18 +386,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)), sc2);
           }
           st_shared_v4(slot + (unit >> 3) * kKChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
-        }
-        if constexpr (kSparse) {
-          // RoPE: staged rows -> 64-byte-swizzled operand chunk
-#pragma unroll
-          for (int it2 = 0; it2 < 2; ++it2) {
-            const int id = it2 * 128 + tid;
-            const int row = id >> 2, u = id & 3;
-            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if ((vmask >> row) & 1ull) v4 = ld_shared_v4f(raw + kRawLat + C::kRawSc + row * 64 + u * 16);
-            st_shared_v4(slot + 4 * kKChunk + row * 64 + ((u ^ ((row >> 1) & 3)) << 4), __float_as_uint(v4.x),
-                         __float_as_uint(v4.y), __float_as_uint(v4.z), __float_as_uint(v4.w));
-          }
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -264,7 +264,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if (!make_map(&tm_kv, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 256, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&tm_sc, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 16, 1, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map(&tm_kvr, kvcache, u8, 1, kvrows, kRowBytesFp8, kRowBytesFp8, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B))
       return MLA_ERR_CUDA;
   } else if (mode == dense::MODE_FP8) {
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
