@@ -49,6 +49,8 @@ WORKLOADS = {
     "fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False),
     "fp8_sparse_b32_sq2_topk2048": dict(kind="sparse", batch=32, s_q=2, topk=2048, causal=False),
     "fp8_sparse_b32_sq2_topk32768": dict(kind="sparse", batch=32, s_q=2, topk=32768, causal=False),
+    # sparse prefill: 1024 query tokens per request, each with its own top-2048 list
+    "fp8_sparse_prefill_b4_sq1024_topk2048": dict(kind="sparse", batch=4, s_q=1024, topk=2048, causal=False),
 }
 SPARSE_TOKENS = 131072
 DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"

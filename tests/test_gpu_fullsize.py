@@ -50,9 +50,15 @@ def _run(w, case, kv, bt, sl, idx):
 
 
 def _samples(B, s_q, n=4, seed=7):
+    """A few requests (first, last, random), and for each every query position
+    when s_q is small, else the first, the last and two random ones."""
     rng = np.random.default_rng(seed)
     bs = sorted(set([0, B - 1] + [int(x) for x in rng.integers(0, B, size=n - 2)]))
-    return [(b, i) for b in bs for i in range(s_q)]
+    out = []
+    for b in bs:
+        qs = range(s_q) if s_q <= 4 else sorted(set([0, s_q - 1] + [int(x) for x in rng.integers(0, s_q, size=2)]))
+        out += [(b, i) for i in qs]
+    return out
 
 
 @pytest.mark.parametrize("workload", ["dense_bf16_b64_sq1_l8192", "dense_bf16_b64_sq1_uniform",
@@ -88,7 +94,8 @@ def test_fp8_dense_full_size_sampled():
         assert_close_attn(out[b, i], lse[b, i], ro, rl, f"fp8 dense b={b}")
 
 
-@pytest.mark.parametrize("workload", ["fp8_sparse_b32_sq2_topk32768", "fp8_sparse_b32_sq1_topk2048"])
+@pytest.mark.parametrize("workload", ["fp8_sparse_b32_sq2_topk32768", "fp8_sparse_b32_sq1_topk2048",
+                                      "fp8_sparse_prefill_b4_sq1024_topk2048"])
 def test_fp8_sparse_full_size_sampled(workload):
     w = bench.WORKLOADS[workload]
     case, _ = bench.build_case(w, DEV)

@@ -287,7 +287,8 @@ def _run_sparse(case, raw_dev, dev="cuda", parts=None):
     return out, lse
 
 
-@pytest.mark.parametrize("s_q,topk,parts", [(1, 256, None), (2, 100, None), (1, 200, 3), (2, 64, 1)])
+@pytest.mark.parametrize("s_q,topk,parts", [(1, 256, None), (2, 100, None), (1, 200, 3), (2, 64, 1),
+                                             (48, 200, None)])
 def test_fp8_sparse(s_q, topk, parts):
     case = synth.make_sparse_case(2, s_q, topk, tokens_per_request=2048, seed=30 + topk, outlier_channels=4)
     dev = "cuda"
