@@ -29,34 +29,42 @@
 // kernel pairs two CTAs over DSM -- Crossover; here the pair exists because
 // TMEM is full.)
 //
-// Memory map. TMEM (512 columns): O half [0,256), S buffers [256,320) and
-// [320,384), and this CTA's 256 latent dims of Q as the UMMA A operand
-// [384,512) (column j = bf16 pair (2j, 2j+1) of head row = lane). Shared
-// memory: the peer's message (E_r fp16 128x64 + m_r + the tile mask, 17 KB),
-// two staged own messages, P (16 KB), the CTA's 32 RoPE dims of Q (8 KB) and a
-// ring of KV tiles (36 KB each: four 64-wide latent chunks, 128-byte swizzled,
-// loaded as one 3-D TMA box, and one 32-wide RoPE chunk, 64-byte swizzled):
-// 4 slots for 16-bit caches, 3 for FP8 caches (whose raw e4m3 rows stage in
-// 2 more slots) and 2 for the sparse mode (3 raw slots, gathered by TMA
-// gather4, four rows per copy).
+// Memory map. TMEM (512 columns): the O half [0,256); S, one buffer
+// [256,320); P of tiles g&1 = 0, 1 at [320,352) and [352,384), 16-bit pairs,
+// read by P . V as its A operand straight from TMEM; and this CTA's 256 latent
+// dims of Q as the A operand of QK^T [384,512) (column j = the 16-bit pair
+// (2j, 2j+1) of head row = lane). Shared memory: the peer's message (E_r fp16
+// 128x64 + m_r + the tile mask, 16.5 KB), this CTA's own message staged for
+// the copy, the CTA's 32 RoPE dims of Q (8 KB) and a ring of KV tiles (36 KB
+// each: four 64-wide latent chunks, 128-byte swizzled, loaded as one 3-D TMA
+// box, and one 32-wide RoPE chunk, 64-byte swizzled): 5 slots for 16-bit
+// caches; 3 for FP8 caches, whose raw e4m3 rows and scales stage in 3 more
+// slots (dense: TMA; sparse: TMA gather4, four rows per copy, with the RoPE
+// dims gathered straight into the operand slot).
 //
 // Warp roles. Warp 0: producer (TMA; the whole warp in the sparse mode).
 // Warp 1: owns TMEM; lane 0 issues QK^T. Warp kPvWarp (2, or 14 for FP8
 // caches): lane 0 issues P . V, so a P . V never waits behind the issue of a
-// QK^T tile. Warps 2-3 and 12-13 (FP8 caches): e4m3 x scale -> fp16 operand
-// tiles. Warps 4-7 (E): read S, form E_r and the row max, stage them and send
-// them to the peer with one bulk shared-to-shared copy; they also copy each
-// piece's Q rows into TMEM. Warps 8-11 (P): receive the peer's message, form
-// P, rescale O when the running max moves by more than 2^8, and write the
-// piece's output. Warp w of the E and P groups serves TMEM lanes (heads)
-// 32*(w%4) .. +31.
+// QK^T tile; it holds a ready P . V back while a QK^T is executing, so that
+// it fills the pipe while the E warps read S instead of delaying S. Warps 2-3
+// and 12-13 (FP8 caches): e4m3 x scale -> fp16 operand tiles. Warps 4-7 (E):
+// read S, form E_r and the row max, stage them and send them to the peer with
+// one bulk shared-to-shared copy; they also copy each piece's Q rows into
+// TMEM. Warps 8-11 (P): receive the peer's message, form P into TMEM, rescale
+// O when the running max moves by more than 2^8, and write the piece's
+// output. Warp w of the E and P groups serves TMEM lanes (heads) 32*(w%4) ..
+// +31.
 //
 // Pipeline. Every hand-off is an mbarrier; every wait is bounded (a wait that
-// gives up sets a status bit and the kernel unwinds). Measured on GB300: a
-// tile's ring slot stays busy from its TMA load through QK^T, the pair
-// exchange (about 1,100 cycles for the 16.5 KB copy), P and P . V, about
-// 9,600 cycles in all, so the tile period is that lifetime over the ring
-// depth; small single-CTA UMMAs cost 50-80 cycles each to issue.
+// gives up sets a status bit and the kernel unwinds). Measured on GB300 with
+// per-tile clock stamps: the tile period (about 2,300 cycles for 16-bit
+// caches) is set by two loops of about that length -- QK^T issue and
+// completion plus the E warps' read of the single S buffer, and the exchange
+// buffers (a 16.5 KB copy between the SMs of a pair lands about 1,250 cycles
+// after it is issued) -- with the ring deep enough to cover the rest. A
+// single-CTA UMMA with N=64 costs as much as one with N=128 (about 64 cycles
+// at M=128, K=16), so QK^T of a tile takes about 1,150 cycles of the tensor
+// pipe and P . V about 512.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -475,9 +483,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           // waits for that S to complete and fills the gap while the E warps
           // read it. S(n-1) is complete once its phase is seen or once QK^T n
           // has started (it waits for S(n-1) to be read); the wait is
-          // bounded, and giving up only changes the order of the MMAs.
+          // bounded, and giving up only changes the order of the MMAs. (The
+          // sparse mode, bound by its gathers and dequantisation, measured
+          // faster without it.)
           const uint32_t n = *qk_started;
-          if (n > 0u) {
+          if (!kSparse && n > 0u) {
             const uint64_t t_0 = cycles();
             while (!mbar_test(bar(C::B_SFULL), (n - 1u) & 1u) && *qk_started == n && cycles() - t_0 < 20000u) {}
           }
