@@ -166,6 +166,24 @@ def dequantize_kv_fp8(raw: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# the per-head GEMMs around attention (weight absorption)
+# ----------------------------------------------------------------------------
+def absorb_q(q_nope, w_uk) -> np.ndarray:
+    """Absorbed query q~_{t,i} = W^UK_i^T q^C_{t,i} ("矩阵、注意力与 GPU：拆解
+    DeepGEMM 与 FlashMLA", §六 '吸收'), so that q~ . c equals q^C . (W^UK c).
+    q_nope [..., h, d_h], w_uk [h, d_h, d_c] -> [..., h, d_c], float64."""
+    return np.einsum("hdc,...hd->...hc", np.asarray(w_uk, np.float64), np.asarray(q_nope, np.float64))
+
+
+def up_project(o_lat, w_uv) -> np.ndarray:
+    """Per-head output o_{t,i} = W^UV_i o~_{t,i} from the attention-weighted
+    latent o~ (same section: the value is W^UV_i c, and the weights sum
+    commutes with W^UV_i). o_lat [..., h, d_c], w_uv [h, d_h, d_c] ->
+    [..., h, d_h], float64."""
+    return np.einsum("hdc,...hc->...hd", np.asarray(w_uv, np.float64), np.asarray(o_lat, np.float64))
+
+
+# ----------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------
 def attend(qh: np.ndarray, keys: np.ndarray, scale: float, d_v: int = _LAT

@@ -7,7 +7,7 @@ softmax or quantisation arithmetic.
 """
 from .workloads import (  # noqa: F401
     D_K, D_V, D_ROPE, FP8_ROW_BYTES,
-    DenseCase, SparseCase,
-    make_dense_case, make_sparse_case, make_latent_rows,
+    DenseCase, SparseCase, AbsorbCase,
+    make_dense_case, make_sparse_case, make_latent_rows, make_absorb_case,
     uniform_seqlens, paged_rows_index,
 )

@@ -178,3 +178,24 @@ def make_sparse_case(batch: int, s_q: int, topk: int, tokens_per_request: int = 
     return SparseCase(q=q, kv_rows=rows, indices=torch.from_numpy(idx),
                       tokens_per_request=tokens_per_request, page_block=page_block,
                       s_q=s_q, h_q=h_q, softmax_scale=D_K ** -0.5)
+
+
+@dataclasses.dataclass
+class AbsorbCase:
+    """Per-head projection weights and activations around the decode kernel:
+    q_nope [T, h, d_h], o_lat [T, h, d_c], w_uk and w_uv [h, d_h, d_c]."""
+    q_nope: torch.Tensor
+    o_lat: torch.Tensor
+    w_uk: torch.Tensor
+    w_uv: torch.Tensor
+
+
+def make_absorb_case(tokens: int, h: int = 128, d_h: int = 128, d_c: int = 512, dtype=torch.bfloat16,
+                     seed: int = 0, device="cpu") -> AbsorbCase:
+    """Activations ~N(0,1); weights ~N(0, 1/fan_in) so that every output is ~N(0,1)
+    (W^UK contracts over d_h, W^UV over d_c). Seeds seed+20 .. seed+23."""
+    def rnd(shape, k, std):
+        g = _gen(seed + 20 + k, device)
+        return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * std).to(dtype)
+    return AbsorbCase(q_nope=rnd((tokens, h, d_h), 0, 1.0), o_lat=rnd((tokens, h, d_c), 1, 1.0),
+                      w_uk=rnd((h, d_h, d_c), 2, d_h ** -0.5), w_uv=rnd((h, d_h, d_c), 3, d_c ** -0.5))

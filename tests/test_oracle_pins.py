@@ -351,8 +351,9 @@ def test_etap_transposed_formulation_matches():
 
 def test_weight_absorption_identity():
     """Naive per-head attention with k_i = [W^UK_i c; k^R], v_i = W^UV_i c equals
-    absorbed q~_i = W^UK_i^T q^C_i scored against [c; k^R], followed by
-    o_i = W^UV_i . (attention-weighted c) (拆解 page §六 '吸收')."""
+    absorbed q~_i = W^UK_i^T q^C_i (oracle.absorb_q) scored against [c; k^R],
+    followed by o_i = W^UV_i . (attention-weighted c) (oracle.up_project)
+    (拆解 page §六 '吸收'). d_h != d_c, so a transposed weight fails by shape."""
     rng = _rng(9)
     n_h, d_h, d_c, d_R, T = 4, 8, 16, 4, 11
     W_UK = rng.standard_normal((n_h, d_h, d_c))
@@ -363,9 +364,9 @@ def test_weight_absorption_identity():
     qR = rng.standard_normal((n_h, d_R))
     sc = (d_h + d_R) ** -0.5
     cache = np.concatenate([c, kR], axis=1)                  # the latent row
-    q_abs = np.concatenate([np.einsum("hdc,hd->hc", W_UK, qC), qR], axis=1)
+    q_abs = np.concatenate([oracle.absorb_q(qC, W_UK), qR], axis=1)
     lat, lse = oracle.attend(q_abs, cache, sc, d_v=d_c)
-    o_abs = np.einsum("hdc,hc->hd", W_UV, lat)
+    o_abs = oracle.up_project(lat, W_UV)
     for i in range(n_h):
         k_i = np.concatenate([c @ W_UK[i].T, kR], axis=1)   # [T, d_h + d_R]
         v_i = c @ W_UV[i].T                                  # [T, d_h]
@@ -374,6 +375,24 @@ def test_weight_absorption_identity():
         o_naive = (p @ v_i) / p.sum()
         np.testing.assert_allclose(o_abs[i], o_naive, rtol=1e-12, atol=1e-12)
         assert abs(lse[i] - (s.max() + math.log(p.sum()))) < 1e-12
+
+
+def test_absorption_batched_over_tokens():
+    """absorb_q / up_project over a token axis equal the per-token, per-head
+    matrix-vector products written out as loops."""
+    rng = _rng(19)
+    T, n_h, d_h, d_c = 3, 2, 5, 7
+    W_UK = rng.standard_normal((n_h, d_h, d_c))
+    W_UV = rng.standard_normal((n_h, d_h, d_c))
+    qC = rng.standard_normal((T, n_h, d_h))
+    ol = rng.standard_normal((T, n_h, d_c))
+    qa, ou = oracle.absorb_q(qC, W_UK), oracle.up_project(ol, W_UV)
+    for t in range(T):
+        for i in range(n_h):
+            for c in range(d_c):
+                assert abs(qa[t, i, c] - sum(W_UK[i, d, c] * qC[t, i, d] for d in range(d_h))) < 1e-12
+            for d in range(d_h):
+                assert abs(ou[t, i, d] - sum(W_UV[i, d, c] * ol[t, i, c] for c in range(d_c))) < 1e-12
 
 
 # ---------------------------------------------------------------------------
