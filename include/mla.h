@@ -217,6 +217,32 @@ MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, c
 MLA_API mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* stream);
 
 /*
+ * The per-head GEMMs around the kernel ("矩阵、注意力与 GPU：拆解 DeepGEMM 与
+ * FlashMLA", §六 '吸收'): with the key up-projection W^UK_i (d_h x d_c) absorbed
+ * into the query, q~_{t,i} = W^UK_i^T q^C_{t,i}, every head scores the shared
+ * latent row; the value up-projection is applied once to the attention-weighted
+ * latent, o_{t,i} = W^UV_i o~_{t,i}. Here d_h = 128 and d_c = 512; tokens is the
+ * number of query tokens (batch * s_q), h_q the number of heads; dtype is
+ * MLA_DTYPE_BF16 or MLA_DTYPE_FP16 for every operand. Products accumulate in
+ * fp32 and are rounded once to dtype. All pointers are (device), 16-B aligned.
+ *
+ * mla_absorb_q: q_nope [tokens, h_q, 128], w_uk [h_q, 128, 512] (W^UK_i row d
+ * holds the 512 latent weights of output dim d); writes dims [0, 512) of every
+ * row of q_out [tokens, h_q, 576], the layout mla_decode_with_kvcache reads,
+ * and leaves the 64 RoPE dims [512, 576) to the caller.
+ *
+ * mla_up_project: o_lat [tokens, h_q, 512] (the decode output), w_uv
+ * [h_q, 128, 512]; writes o_out [tokens, h_q, 128].
+ *
+ * tokens = 0 enqueues nothing. Returns MLA_ERR_INVALID_ARG for a negative size,
+ * a null or misaligned pointer, or an unknown dtype.
+ */
+MLA_API mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int tokens, int h_q, int dtype,
+                                void* stream);
+MLA_API mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_out, int tokens, int h_q, int dtype,
+                                  void* stream);
+
+/*
  * Synchronise `stream`, read and clear the status word of `workspace`, and
  * return the first error it records (MLA_OK if none). *bits (optional)
  * receives the raw bits: 1 = index/page skipped, 2 = wait timeout,

@@ -69,6 +69,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.mla_quantize_kv_fp8.argtypes = [vp, vp, c.c_int64, vp]
         lib.mla_read_status.restype = c.c_int
         lib.mla_read_status.argtypes = [vp, vp, c.POINTER(c.c_uint32)]
+        for name in ("mla_absorb_q", "mla_up_project"):
+            f = getattr(lib, name)
+            f.restype = c.c_int
+            f.argtypes = [vp, vp, vp, c.c_int, c.c_int, c.c_int, vp]
         if path is None:
             _lib = lib
         return lib
@@ -239,6 +243,48 @@ def mla_quantize_kv_fp8(kv: torch.Tensor, out: Optional[torch.Tensor] = None) ->
     st = lib.mla_quantize_kv_fp8(_ptr(kv), _ptr(out), n, _stream(kv.device))
     _check(st, "mla_quantize_kv_fp8")
     return out
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return 0
+    if t.dtype == torch.float16:
+        return 1
+    raise MLAError(1, f"unsupported dtype {t.dtype}")
+
+
+def mla_absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """q~ = W^UK_i^T q^C per head: q_nope [..., h, 128], w_uk [h, 128, 512] ->
+    dims [0, 512) of q_out [..., h, 576] (allocated if not given; its RoPE dims
+    are the caller's)."""
+    lib = load_library()
+    h = q_nope.shape[-2]
+    assert q_nope.shape[-1] == 128 and tuple(w_uk.shape) == (h, 128, 512)
+    assert q_nope.is_contiguous() and w_uk.is_contiguous() and w_uk.dtype == q_nope.dtype
+    tokens = q_nope.numel() // (h * 128)
+    if q_out is None:
+        q_out = torch.zeros(*q_nope.shape[:-1], 576, dtype=q_nope.dtype, device=q_nope.device)
+    assert q_out.is_contiguous() and q_out.dtype == q_nope.dtype and q_out.numel() == tokens * h * 576
+    st = lib.mla_absorb_q(_ptr(q_nope), _ptr(w_uk), _ptr(q_out), tokens, h, _dtype_code(q_nope),
+                          _stream(q_nope.device))
+    _check(st, "mla_absorb_q")
+    return q_out
+
+
+def mla_up_project(o_lat: torch.Tensor, w_uv: torch.Tensor, o_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """o = W^UV_i o~ per head: o_lat [..., h, 512], w_uv [h, 128, 512] -> [..., h, 128]."""
+    lib = load_library()
+    h = o_lat.shape[-2]
+    assert o_lat.shape[-1] == 512 and tuple(w_uv.shape) == (h, 128, 512)
+    assert o_lat.is_contiguous() and w_uv.is_contiguous() and w_uv.dtype == o_lat.dtype
+    tokens = o_lat.numel() // (h * 512)
+    if o_out is None:
+        o_out = torch.empty(*o_lat.shape[:-1], 128, dtype=o_lat.dtype, device=o_lat.device)
+    assert o_out.is_contiguous() and o_out.dtype == o_lat.dtype and o_out.numel() == tokens * h * 128
+    st = lib.mla_up_project(_ptr(o_lat), _ptr(w_uv), _ptr(o_out), tokens, h, _dtype_code(o_lat),
+                            _stream(o_lat.device))
+    _check(st, "mla_up_project")
+    return o_out
 
 
 def mla_read_status(workspace: Optional[torch.Tensor] = None, device=None) -> Tuple[int, int]:

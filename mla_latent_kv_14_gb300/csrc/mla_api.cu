@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/mla.h"
+#include "absorb.cuh"
 #include "decode_dense.cuh"
 #include "decode_fewheads.cuh"
 #include "params.h"
@@ -77,6 +78,17 @@ bool make_map_chunks(CUtensorMap* m, const void* base, CUtensorMapDataType dt, u
   cuuint32_t box[3] = {64, box_rows, box_chunks};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 4-D 16-bit tensor map with 128-byte swizzle (the inner box is 64
+// elements = 128 B); strides in bytes for dims 1..3.
+bool make_map_4d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, const cuuint64_t (&dims)[4],
+                 const cuuint64_t (&strides)[3], const cuuint32_t (&box)[4]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -402,6 +414,66 @@ mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* st
   const int64_t want = (n + 7) / 8;
   const int grid = (int)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
   mla_quant_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(kv), out, n);
+  MLA_CUDA(cudaGetLastError());
+  return MLA_OK;
+}
+
+mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int tokens, int h_q, int dtype,
+                        void* stream) {
+  if (tokens < 0 || h_q < 1 || (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16)) return MLA_ERR_INVALID_ARG;
+  if (tokens == 0) return MLA_OK;
+  if (!q_nope || !w_uk || !q_out || !aligned(q_nope, 16) || !aligned(w_uk, 16) || !aligned(q_out, 16))
+    return MLA_ERR_INVALID_ARG;
+  const CUtensorMapDataType dt =
+      dtype == MLA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t H = (cuuint64_t)h_q, T = (cuuint64_t)tokens;
+  // q_nope [T, h, 128] as {64 dims, tokens, 2 chunks, heads}: tiles [chunk][token][64]
+  CUtensorMap tm_a, tm_b;
+  if (!make_map_4d(&tm_a, q_nope, dt, {64, T, 2, H}, {H * 256, 128, 256}, {64, absorb::kTokTile, 2, 1}) ||
+      // w_uk [h, 128, 512] as {64 latent dims, 128 rows, 8 chunks, heads}: [chunk][row][64]
+      !make_map_4d(&tm_b, w_uk, dt, {64, 128, 8, H}, {1024, 128, 128 * 1024}, {64, 128, 8, 1}))
+    return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 grid((unsigned)h_q, (unsigned)((tokens + absorb::kTokTile - 1) / absorb::kTokTile));
+  if (dtype == MLA_DTYPE_FP16) {
+    MLA_CUDA(set_smem(absorb::mla_absorb_q_kernel<true>, absorb::kAbsorbSmem));
+    absorb::mla_absorb_q_kernel<true><<<grid, absorb::kThreads, absorb::kAbsorbSmem, st>>>(tm_a, tm_b, q_out, tokens,
+                                                                                           h_q, nullptr);
+  } else {
+    MLA_CUDA(set_smem(absorb::mla_absorb_q_kernel<false>, absorb::kAbsorbSmem));
+    absorb::mla_absorb_q_kernel<false><<<grid, absorb::kThreads, absorb::kAbsorbSmem, st>>>(tm_a, tm_b, q_out, tokens,
+                                                                                            h_q, nullptr);
+  }
+  MLA_CUDA(cudaGetLastError());
+  return MLA_OK;
+}
+
+mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_out, int tokens, int h_q, int dtype,
+                          void* stream) {
+  if (tokens < 0 || h_q < 1 || (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16)) return MLA_ERR_INVALID_ARG;
+  if (tokens == 0) return MLA_OK;
+  if (!o_lat || !w_uv || !o_out || !aligned(o_lat, 16) || !aligned(w_uv, 16) || !aligned(o_out, 16))
+    return MLA_ERR_INVALID_ARG;
+  const CUtensorMapDataType dt =
+      dtype == MLA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t H = (cuuint64_t)h_q, T = (cuuint64_t)tokens;
+  // o_lat [T, h, 512] as {64 dims, tokens, 8 chunks, heads}: tiles [chunk][token][64]
+  CUtensorMap tm_a, tm_b;
+  if (!make_map_4d(&tm_a, o_lat, dt, {64, T, 8, H}, {H * 1024, 128, 1024}, {64, absorb::kTokTile, 4, 1}) ||
+      // w_uv [h, 128, 512] as {64 latent dims, 128 rows, 8 chunks, heads}: [chunk][row][64]
+      !make_map_4d(&tm_b, w_uv, dt, {64, 128, 8, H}, {1024, 128, 128 * 1024}, {64, 128, 4, 1}))
+    return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 grid((unsigned)h_q, (unsigned)((tokens + absorb::kTokTile - 1) / absorb::kTokTile));
+  if (dtype == MLA_DTYPE_FP16) {
+    MLA_CUDA(set_smem(absorb::mla_up_project_kernel<true>, absorb::kUpSmem));
+    absorb::mla_up_project_kernel<true><<<grid, absorb::kThreads, absorb::kUpSmem, st>>>(tm_a, tm_b, o_out, tokens,
+                                                                                         h_q, nullptr);
+  } else {
+    MLA_CUDA(set_smem(absorb::mla_up_project_kernel<false>, absorb::kUpSmem));
+    absorb::mla_up_project_kernel<false><<<grid, absorb::kThreads, absorb::kUpSmem, st>>>(tm_a, tm_b, o_out, tokens,
+                                                                                          h_q, nullptr);
+  }
   MLA_CUDA(cudaGetLastError());
   return MLA_OK;
 }
