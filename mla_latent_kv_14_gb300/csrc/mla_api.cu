@@ -209,8 +209,24 @@ mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, in
   if (smem > 48 * 1024) {
     MLA_CUDA(cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   }
-  mla_metadata_kernel<<<1, kMetaThreads, smem, static_cast<cudaStream_t>(stream)>>>(mp);
-  MLA_CUDA(cudaGetLastError());
+  // one block; small problems use fewer threads (cheaper block-wide scans)
+  const int need = (batch * s_q > parts ? batch * s_q : parts);
+  int threads = (need + 31) / 32 * 32;
+  threads = threads < 128 ? 128 : (threads > kMetaThreads ? kMetaThreads : threads);
+  // launched as a programmatic dependent of whatever precedes it on the stream
+  // (e.g. the previous call's combine); the kernel waits for it before any
+  // global access, so only the launch latency is overlapped
+  cudaLaunchConfig_t mc = {};
+  mc.gridDim = dim3(1, 1, 1);
+  mc.blockDim = dim3((unsigned)threads, 1, 1);
+  mc.dynamicSmemBytes = smem;
+  mc.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute mat[1];
+  mat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  mat[0].val.programmaticStreamSerializationAllowed = 1;
+  mc.attrs = mat;
+  mc.numAttrs = 1;
+  MLA_CUDA(cudaLaunchKernelEx(&mc, mla_metadata_kernel, mp));
   return MLA_OK;
 }
 

@@ -101,6 +101,10 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 //    other than its first.
 __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p) {
   pdl_launch_dependents();  // the decode may start its set-up now; it waits for this grid before reading
+  // This grid may itself be launched early, behind the previous call's
+  // combine, which still reads the buffers written here: wait for it (and for
+  // whatever produced the lengths) before the first global access.
+  pdl_wait();
   extern __shared__ long long sh[];
   const int V = p.batch * p.s_q;
   long long* C = sh;                                        // [V + 1]
@@ -357,6 +361,7 @@ struct MaskStream {
 // two splits are in flight at a time.
 template <typename OutT>
 __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
+  pdl_launch_dependents();  // a following schedule kernel may launch; it waits for this grid
   pdl_wait();  // the decode grid has completed and its writes are visible
   const int v = blockIdx.x;
   const int b = v % p.batch, i = v / p.batch;
