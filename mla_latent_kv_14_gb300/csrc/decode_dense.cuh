@@ -202,20 +202,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     tmem_alloc(smem_u32(misc), kTmemCols);
     tmem_relinquish();
   }
-  // Everything above reads no global memory. The schedule, and possibly the
-  // query, cache and tables, come from kernels earlier on the stream; the
-  // launch is a programmatic dependent launch, so wait for them here.
-  pdl_wait();
-  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
-  if (threadIdx.x == 0) {
-    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
-    if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) fence_mbar_init();
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before any remote access
   tc_fence_after();
+  // Everything above reads no global memory. The schedule, and possibly the
+  // query, cache and tables, come from kernels earlier on the stream; the
+  // launch is a programmatic dependent launch, so wait for them here. The
+  // metadata header is loaded before the lengths are hashed, so that both
+  // reads are in flight together.
+  pdl_wait();
+  int32_t hdr[H_WORDS];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < H_WORDS; ++k) hdr[k] = p.meta[k];
+  }
+  const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
+  if (threadIdx.x == 0) {
+    *ok_flag = header_matches(hdr, p, kTile, fp) ? 1u : 0u;
+    if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
+  }
+  __syncthreads();
   const uint32_t tmem = *tmem_slot;
   const bool ok = *ok_flag != 0u;
 

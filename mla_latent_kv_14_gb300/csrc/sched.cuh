@@ -222,6 +222,15 @@ __device__ __forceinline__ bool metadata_matches(const DecodeParams& p, int page
          h[H_PARTS] == p.parts && h[H_VREQ] == p.batch * p.s_q && (uint32_t)h[H_HASH] == fp;
 }
 
+// The same check on a header already loaded into registers (all comparisons
+// evaluated, so the loads can all be in flight together).
+__device__ __forceinline__ bool header_matches(const int32_t (&h)[H_WORDS], const DecodeParams& p, int page_block,
+                                               uint32_t fp) {
+  return (h[H_MAGIC] == kMetaMagic) & (h[H_BATCH] == p.batch) & (h[H_SQ] == p.s_q) & (h[H_HQ] == p.h_q) &
+         (h[H_TOPK] == p.topk) & (h[H_FP8] == p.is_fp8) & (h[H_CAUSAL] == p.causal) & (h[H_PAGE] == page_block) &
+         (h[H_PARTS] == p.parts) & (h[H_VREQ] == p.batch * p.s_q) & ((uint32_t)h[H_HASH] == fp);
+}
+
 // Iteration over the pieces of one SM part: every role of a decode kernel
 // walks the same list of (virtual request, tile range) pieces.
 struct Piece {
