@@ -385,7 +385,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   // combine, overlapped with the decode grid's tail (programmatic dependent launch)
   CombineParams c{num_splits, p.o_part, p.lse_part, out, lse, batch, s_q, h_q, fp16 ? 1 : 0};
   cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(batch * s_q, (h_q + 7) / 8, 1);
+  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, 1);
   cc.blockDim = dim3(256, 1, 1);
   cc.stream = st;
   cudaLaunchAttribute at[1];

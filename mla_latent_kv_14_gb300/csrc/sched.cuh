@@ -362,8 +362,8 @@ struct MaskStream {
   }
 };
 
-// Merge the split partials of each virtual request. grid = (vreq, h_q/8),
-// block = 256: each warp merges one head, each lane 16 of the 512 dims.
+// Merge the split partials of each virtual request. grid = (vreq, h_q/16),
+// block = 256: each warp merges two heads, each lane 16 of the 512 dims.
 // Requests with a single piece were finished by the decode kernel; requests
 // with no visible token get out = 0, lse = -inf here. Lane s holds the lse
 // (and weight) of split s, so the weights take one load; the partial rows of
@@ -378,64 +378,66 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   const int ns = p.split_off[v + 1] - off;
   if (ns == 1) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 8 + warp;
-  if (h >= p.h_q) return;
-  const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
-  OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
-  auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };
-  float mx = -INFINITY;
-  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, lse_at(s));
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = blockIdx.y * 16 + warp * 2 + hh;
+    if (h >= p.h_q) break;
+    const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
+    OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
+    auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, lse_at(s));
 #pragma unroll
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float acc[16];
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[16];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      const float ls = s0 + lane < ns ? lse_at(s0 + lane) : -INFINITY;
-      const float w_l = ls == -INFINITY ? 0.f : expf(ls - mx);
-      const int cnt = ns - s0 < 32 ? ns - s0 : 32;
-      for (int k = 0; k < cnt; k += 2) {
-        const bool two = k + 1 < cnt;
-        const float4* sa = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k) * p.h_q + h) * kDV);
-        const float4* sbp = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k + (two ? 1 : 0)) * p.h_q + h) * kDV);
-        float4 xa[4], xb[4];
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int s0 = 0; s0 < ns; s0 += 32) {
+        const float ls = s0 + lane < ns ? lse_at(s0 + lane) : -INFINITY;
+        const float w_l = ls == -INFINITY ? 0.f : expf(ls - mx);
+        const int cnt = ns - s0 < 32 ? ns - s0 : 32;
+        for (int k = 0; k < cnt; k += 2) {
+          const bool two = k + 1 < cnt;
+          const float4* sa = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k) * p.h_q + h) * kDV);
+          const float4* sbp = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k + (two ? 1 : 0)) * p.h_q + h) * kDV);
+          float4 xa[4], xb[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xa[j] = sa[j * 32 + lane];
-          xb[j] = sbp[j * 32 + lane];
-        }
-        const float wa = __shfl_sync(0xffffffffu, w_l, k);
-        const float wb = two ? __shfl_sync(0xffffffffu, w_l, (k + 1) & 31) : 0.f;
-        wsum += wa + wb;
+          for (int j = 0; j < 4; ++j) {
+            xa[j] = sa[j * 32 + lane];
+            xb[j] = sbp[j * 32 + lane];
+          }
+          const float wa = __shfl_sync(0xffffffffu, w_l, k);
+          const float wb = two ? __shfl_sync(0xffffffffu, w_l, (k + 1) & 31) : 0.f;
+          wsum += wa + wb;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[4 * j + 0] += wa * xa[j].x + wb * xb[j].x;
-          acc[4 * j + 1] += wa * xa[j].y + wb * xb[j].y;
-          acc[4 * j + 2] += wa * xa[j].z + wb * xb[j].z;
-          acc[4 * j + 3] += wa * xa[j].w + wb * xb[j].w;
+          for (int j = 0; j < 4; ++j) {
+            acc[4 * j + 0] += wa * xa[j].x + wb * xb[j].x;
+            acc[4 * j + 1] += wa * xa[j].y + wb * xb[j].y;
+            acc[4 * j + 2] += wa * xa[j].z + wb * xb[j].z;
+            acc[4 * j + 3] += wa * xa[j].w + wb * xb[j].w;
+          }
         }
       }
     }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int d = j * 128 + lane * 4;
-    if constexpr (sizeof(OutT) == 2) {
-      uint32_t lo, hi;
-      if constexpr (std::is_same<OutT, __half>::value) {
-        lo = pack_f16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
-        hi = pack_f16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
-      } else {
-        lo = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
-        hi = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+    for (int j = 0; j < 4; ++j) {
+      const int d = j * 128 + lane * 4;
+      if constexpr (sizeof(OutT) == 2) {
+        uint32_t lo, hi;
+        if constexpr (std::is_same<OutT, __half>::value) {
+          lo = pack_f16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
+          hi = pack_f16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+        } else {
+          lo = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
+          hi = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
+        }
+        *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
       }
-      *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
     }
+    if (lane == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
-  if (lane == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace mla
