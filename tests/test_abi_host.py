@@ -29,6 +29,7 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for must in ["mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits", "mla_quantize_kv_fp8", "mla_read_status",
+                 "mla_absorb_q", "mla_up_project", "mla_decode_with_kvcache_noalloc",
                  "mla_metadata_size", "mla_workspace_size", "mla_num_sm_parts", "mla_status_string"]:
         assert must in names
 
@@ -103,3 +104,21 @@ def test_quantize_argument_checks(lib):
     assert lib.mla_quantize_kv_fp8(FAKE, FAKE, -1, None) == 1
     assert lib.mla_quantize_kv_fp8(ctypes.c_void_p((1 << 20) + 8), FAKE, 4, None) == 1
     assert lib.mla_quantize_kv_fp8(FAKE, FAKE, 0, None) == 0
+
+
+@pytest.mark.parametrize("name", ["mla_absorb_q", "mla_up_project"])
+def test_absorption_argument_checks(lib, name):
+    """Bad sizes, dtypes, null or misaligned pointers are rejected before any
+    device call; tokens = 0 is a no-op."""
+    f = getattr(lib, name)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    assert f(FAKE, FAKE, FAKE, -1, 128, 0, None) == 1          # negative token count
+    assert f(FAKE, FAKE, FAKE, 4, 0, 0, None) == 1             # no heads
+    assert f(FAKE, FAKE, FAKE, 4, 128, 7, None) == 1           # unknown dtype
+    assert f(None, FAKE, FAKE, 4, 128, 0, None) == 1           # null input
+    assert f(FAKE, None, FAKE, 4, 128, 0, None) == 1           # null weights
+    assert f(FAKE, FAKE, None, 4, 128, 0, None) == 1           # null output
+    assert f(mis, FAKE, FAKE, 4, 128, 0, None) == 1            # misaligned input
+    assert f(FAKE, mis, FAKE, 4, 128, 1, None) == 1            # misaligned weights
+    assert f(FAKE, FAKE, mis, 4, 128, 0, None) == 1            # misaligned output
+    assert f(None, None, None, 0, 128, 0, None) == 0           # nothing to do
