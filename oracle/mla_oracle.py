@@ -22,7 +22,7 @@ What it computes, and where the pages say so
   fp32 scales, then the 64 RoPE dims kept as bf16; 656 bytes ("FlashMLA 实战",
   §FP8 缓存怎么把 KV 压掉四成; 拆解 page §八 '格式').
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
 * causal with s_q > 1 is bottom-right aligned: query i of s_q sees tokens
   t <= L - s_q + i;
 * an empty visible set gives out = 0 and lse = -inf;
