@@ -52,7 +52,8 @@ typedef enum {
   MLA_ERR_STALE_METADATA = 3,   /* metadata computed for a different shape/lengths */
   MLA_ERR_INDEX = 4,            /* an out-of-range page or sparse index was skipped */
   MLA_ERR_TIMEOUT = 5,          /* a device pipeline wait gave up (kernel returned early) */
-  MLA_ERR_CUDA = 6              /* a CUDA runtime/driver call failed */
+  MLA_ERR_CUDA = 6,             /* a CUDA runtime/driver call failed */
+  MLA_ERR_RANGE = 7             /* FP8 path: a value beyond fp16 range was saturated (see below) */
 } mla_status;
 
 typedef enum { MLA_DTYPE_BF16 = 0, MLA_DTYPE_FP16 = 1 } mla_dtype;
@@ -132,6 +133,14 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * workspace    (device) mla_workspace_size() bytes, 256-B aligned; its status
  *              word must be zeroed once before first use (mla_read_status clears it).
  * A request with no visible token gets out = 0 and lse = -inf.
+ * FP8 caches (is_fp8 = 1) run the latent product in fp16: the bf16 query is
+ * rounded to fp16 and each cache value is formed as fp16(code) x fp16(block
+ * scale), rounded to fp16. Within range the dequantised value has relative
+ * error <= 2^-10; a block whose amax is below 448 * 2^-14 (~0.027) has an
+ * fp16-subnormal scale, and its values carry an absolute error <= 2^-15
+ * instead. Out of range -- a query entry beyond 65504 in magnitude (saturated
+ * to +-65504) or a block scale above 146 (block amax above 65408) -- the
+ * status word records MLA_ERR_RANGE.
  * h_q = 128 with any cache; h_q = 16 with a dense 16-bit cache only: the few
  * heads fill the MMA's N dimension and the 64 tokens of a tile its M
  * dimension, the transposed formulation S^T = K Q^T, O^T = V^T P^T of the
@@ -193,7 +202,7 @@ MLA_API mla_status mla_combine_splits(const void* q, int q_dtype, const void* kv
  *    capture;
  *  - status (device, optional, 4-B aligned): receives the device-side status
  *    bits of this call (1 = index/page skipped, 2 = wait timeout, 4 = stale
- *    metadata), or NULL to discard them.
+ *    metadata, 8 = FP8 range), or NULL to discard them.
  */
 MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, const void* kvcache,
                                                    int64_t num_blocks, int page_block,
@@ -234,21 +243,39 @@ MLA_API mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, 
  * mla_up_project: o_lat [tokens, h_q, 512] (the decode output), w_uv
  * [h_q, 128, 512]; writes o_out [tokens, h_q, 128].
  *
+ * status (device, optional, 4-B aligned): a status word the kernels OR bit 2
+ * (wait timeout) into when a bounded wait gave up (nothing is stored then);
+ * read and clear it with mla_read_status(). NULL discards it.
+ *
  * tokens = 0 enqueues nothing. Returns MLA_ERR_INVALID_ARG for a negative size,
  * a null or misaligned pointer, or an unknown dtype.
  */
 MLA_API mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int tokens, int h_q, int dtype,
-                                void* stream);
+                                uint32_t* status, void* stream);
 MLA_API mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_out, int tokens, int h_q, int dtype,
-                                  void* stream);
+                                  uint32_t* status, void* stream);
 
 /*
- * Synchronise `stream`, read and clear the status word of `workspace`, and
- * return the first error it records (MLA_OK if none). *bits (optional)
- * receives the raw bits: 1 = index/page skipped, 2 = wait timeout,
- * 4 = stale metadata.
+ * Synchronise `stream`, read and clear the status word of `workspace` (or of
+ * any 4-B status word, e.g. the one given to mla_absorb_q), and return the
+ * first error it records, in the order timeout, stale metadata, index, range
+ * (MLA_OK if none). *bits (optional) receives the raw bits: 1 = index/page
+ * skipped, 2 = wait timeout, 4 = stale metadata, 8 = FP8 range.
  */
 MLA_API mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits);
+
+/*
+ * Test hook for the time-out path (0, the default, turns it off). While it is
+ * non-zero, every decode kernel (mla_decode_with_kvcache and its variants)
+ * and absorption kernel (mla_absorb_q, mla_up_project) launched by this
+ * library first has one thread per CTA wait `cycles` SM cycles on a barrier
+ * that nothing arrives at, before any copy or MMA is issued; the wait gives up, the kernel records the wait
+ * time-out (status bit 2, MLA_ERR_TIMEOUT) and the CTA skips its work, so the
+ * outputs of those launches are undefined. Process-wide; not for production
+ * use. The pages describe no such hook: it exists so that a test can check that
+ * a device wait which runs out is reported and leaves the context usable.
+ */
+MLA_API void mla_set_test_stall(uint32_t cycles);
 
 #ifdef __cplusplus
 }

@@ -7,5 +7,5 @@ from .binding import (  # noqa: F401
     LIB_PATH, MLAError, Metadata, load_library,
     mla_num_sm_parts, mla_get_metadata, mla_decode_with_kvcache, mla_decode_splitkv, mla_combine_splits,
     mla_decode_with_kvcache_noalloc, mla_quantize_kv_fp8, mla_read_status, workspace_for,
-    mla_absorb_q, mla_up_project,
+    mla_absorb_q, mla_up_project, mla_set_test_stall,
 )

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 MLA_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "stale metadata",
-                4: "out-of-range page or index skipped", 5: "device wait timed out", 6: "CUDA error"}
+                4: "out-of-range page or index skipped", 5: "device wait timed out", 6: "CUDA error",
+                7: "FP8 path: a value beyond fp16 range was saturated"}
 DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1}
 
 _lib = None
@@ -72,7 +73,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         for name in ("mla_absorb_q", "mla_up_project"):
             f = getattr(lib, name)
             f.restype = c.c_int
-            f.argtypes = [vp, vp, vp, c.c_int, c.c_int, c.c_int, vp]
+            f.argtypes = [vp, vp, vp, c.c_int, c.c_int, c.c_int, vp, vp]
+        lib.mla_set_test_stall.restype = None
+        lib.mla_set_test_stall.argtypes = [c.c_uint32]
         if path is None:
             _lib = lib
         return lib
@@ -253,10 +256,12 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise MLAError(1, f"unsupported dtype {t.dtype}")
 
 
-def mla_absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+def mla_absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q_out: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None) -> torch.Tensor:
     """q~ = W^UK_i^T q^C per head: q_nope [..., h, 128], w_uk [h, 128, 512] ->
     dims [0, 512) of q_out [..., h, 576] (allocated if not given; its RoPE dims
-    are the caller's)."""
+    are the caller's). ``status``: optional device status word (read it with
+    :func:`mla_read_status`)."""
     lib = load_library()
     h = q_nope.shape[-2]
     assert q_nope.shape[-1] == 128 and tuple(w_uk.shape) == (h, 128, 512)
@@ -265,14 +270,16 @@ def mla_absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q_out: Optional[torch
     if q_out is None:
         q_out = torch.zeros(*q_nope.shape[:-1], 576, dtype=q_nope.dtype, device=q_nope.device)
     assert q_out.is_contiguous() and q_out.dtype == q_nope.dtype and q_out.numel() == tokens * h * 576
-    st = lib.mla_absorb_q(_ptr(q_nope), _ptr(w_uk), _ptr(q_out), tokens, h, _dtype_code(q_nope),
+    st = lib.mla_absorb_q(_ptr(q_nope), _ptr(w_uk), _ptr(q_out), tokens, h, _dtype_code(q_nope), _ptr(status),
                           _stream(q_nope.device))
     _check(st, "mla_absorb_q")
     return q_out
 
 
-def mla_up_project(o_lat: torch.Tensor, w_uv: torch.Tensor, o_out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """o = W^UV_i o~ per head: o_lat [..., h, 512], w_uv [h, 128, 512] -> [..., h, 128]."""
+def mla_up_project(o_lat: torch.Tensor, w_uv: torch.Tensor, o_out: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """o = W^UV_i o~ per head: o_lat [..., h, 512], w_uv [h, 128, 512] -> [..., h, 128].
+    ``status``: optional device status word (read it with :func:`mla_read_status`)."""
     lib = load_library()
     h = o_lat.shape[-2]
     assert o_lat.shape[-1] == 512 and tuple(w_uv.shape) == (h, 128, 512)
@@ -281,7 +288,7 @@ def mla_up_project(o_lat: torch.Tensor, w_uv: torch.Tensor, o_out: Optional[torc
     if o_out is None:
         o_out = torch.empty(*o_lat.shape[:-1], 128, dtype=o_lat.dtype, device=o_lat.device)
     assert o_out.is_contiguous() and o_out.dtype == o_lat.dtype and o_out.numel() == tokens * h * 128
-    st = lib.mla_up_project(_ptr(o_lat), _ptr(w_uv), _ptr(o_out), tokens, h, _dtype_code(o_lat),
+    st = lib.mla_up_project(_ptr(o_lat), _ptr(w_uv), _ptr(o_out), tokens, h, _dtype_code(o_lat), _ptr(status),
                             _stream(o_lat.device))
     _check(st, "mla_up_project")
     return o_out
@@ -296,3 +303,10 @@ def mla_read_status(workspace: Optional[torch.Tensor] = None, device=None) -> Tu
     bits = ctypes.c_uint32(0)
     st = lib.mla_read_status(_ptr(workspace), _stream(dev), ctypes.byref(bits))
     return st, int(bits.value)
+
+
+def mla_set_test_stall(cycles: int) -> None:
+    """Test hook of the time-out path: while non-zero, every decode and
+    absorption launch first waits ``cycles`` SM cycles on a barrier nothing
+    arrives at, records a wait time-out and skips its work. 0 turns it off."""
+    load_library().mla_set_test_stall(int(cycles))

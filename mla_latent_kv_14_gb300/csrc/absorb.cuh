@@ -16,7 +16,10 @@
 // (M = 128 tokens) into TMEM; the four warps then read their 32 token rows
 // back and store them as 16-bit values. Tokens past T are zero-filled by the
 // copy and not stored. Every wait is bounded; a wait that gives up sets the
-// status word (if one is given) and nothing is stored.
+// status word (if one is given) and nothing is stored. A copy whose wait gave
+// up is waited for once more before the CTA exits. `stall` (a test hook, 0 in
+// normal use) makes thread 0 first wait that many cycles on a barrier nothing
+// arrives at, so the wait gives up before any copy is issued.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -46,10 +49,10 @@ __device__ __forceinline__ void store_row32(void* dst, const uint32_t* r) {
   for (int k = 0; k < 4; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit = kLimit) {
   const uint64_t t0 = cycles();
   while (!mbar_try_wait(bar, parity))
-    if (cycles() - t0 > kLimit) return false;
+    if (cycles() - t0 > limit) return false;
   return true;
 }
 
@@ -60,18 +63,19 @@ constexpr uint32_t kAbsorbSmem = 2 * kChunk + 8 * kChunk + 64 + 1024;
 template <bool kFp16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_absorb_q_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                        void* q_out, int T, int h, uint32_t* status) {
+                        void* q_out, int T, int h, uint32_t* status, uint32_t stall) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_s = sb, b_s = sb + 2 * kChunk;
-  const uint32_t bar_full = sb + 10 * kChunk, bar_done = bar_full + 8;
+  const uint32_t bar_full = sb + 10 * kChunk, bar_done = bar_full + 8, bar_stall = bar_full + 32;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + 10 * kChunk + 16);
   const int head = blockIdx.x, t0 = blockIdx.y * kTokTile;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(bar_full, 1);
     mbar_init(bar_done, 1);
+    mbar_init(bar_stall, 1);
     misc[1] = 1u;  // ok
     fence_mbar_init();
   }
@@ -83,7 +87,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && stall && !wait_bounded(bar_stall, 0, stall)) {
+    misc[1] = 0u;  // test hook: nothing is issued
+    if (status) atomicOr(status, STATUS_TIMEOUT);
+    umma_commit(bar_done);
+  } else if (threadIdx.x == 0) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     mbar_arrive_expect_tx(bar_full, 10 * kChunk);
@@ -92,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_bounded(bar_full, 0)) {
       misc[1] = 0u;
       if (status) atomicOr(status, STATUS_TIMEOUT);
+      (void)wait_bounded(bar_full, 0);  // do not exit with the copy in flight
     } else {
       tc_fence_after();
       constexpr uint32_t idesc = idesc_f16(128, 256, !kFp16, false, true);
@@ -144,13 +153,13 @@ constexpr uint32_t kUpSmem = 8 * kChunk + 64 + 1024;  // + barriers and the TMEM
 template <bool kFp16>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_up_project_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                          void* o_out, int T, int h, uint32_t* status) {
+                          void* o_out, int T, int h, uint32_t* status, uint32_t stall) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_s = sb, b_s = sb + 4 * kChunk;
   // bar_done + 8*half: the MMAs of that half of the contraction are done
-  const uint32_t bar_full = sb + 8 * kChunk, bar_done = bar_full + 8;
+  const uint32_t bar_full = sb + 8 * kChunk, bar_done = bar_full + 8, bar_stall = bar_full + 40;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + 8 * kChunk + 24);
   const int head = blockIdx.x, t0 = blockIdx.y * kTokTile;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -158,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_full, 1);
     mbar_init(bar_done, 1);
     mbar_init(bar_done + 8, 1);
+    mbar_init(bar_stall, 1);
     misc[1] = 1u;
     fence_mbar_init();
   }
@@ -173,14 +183,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     constexpr uint32_t idesc = idesc_f16(128, 128, !kFp16, false, false);
-    bool ok = true;
+    // test hook: a wait that gives up before anything is issued
+    bool ok = !(stall && !wait_bounded(bar_stall, 0, stall));
     for (int half = 0; half < 2 && ok; ++half) {
       // the buffer is free once the first half's MMAs are done
       if (half == 1 && !wait_bounded(bar_done, 0)) { ok = false; break; }
       mbar_arrive_expect_tx(bar_full, 8 * kChunk);
       tma_load_4d(a_s, &tm_a, bar_full, 0, t0, 4 * half, head);
       tma_load_4d(b_s, &tm_b, bar_full, 0, 0, 4 * half, head);
-      if (!wait_bounded(bar_full, half)) { ok = false; break; }
+      if (!wait_bounded(bar_full, half)) {
+        ok = false;
+        (void)wait_bounded(bar_full, half);  // do not exit with the copy in flight
+        break;
+      }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {

@@ -92,7 +92,15 @@ constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 3
 constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
 constexpr uint32_t kXM = kXE;                           // + m_r per row (fp32)
 constexpr uint32_t kXMask = kXM + 128 * 4;              // + validity mask of the tile (64 bits)
+constexpr uint32_t kXFlag = kXMask + 8;                 // + 1 if this half of the tile is wide
 constexpr uint32_t kXBytes = kXMask + 16;
+// a wide half follows its message with two more: fp32 s_r - m_r of rows
+// 0-63, then of rows 64-127 (256 B per row)
+constexpr uint32_t kXPart = 64 * 256;
+// E_r = 2^(s_r - m_r + kEShift): fp16's normal range then holds every token
+// within kNarrow binades of the half's own maximum (2^-13 .. 2^15)
+constexpr float kEShift = 15.0f;
+constexpr float kNarrow = 28.0f;
 constexpr uint32_t kXStride = 17 * 1024;
 constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
@@ -125,7 +133,7 @@ struct Cfg {
                             B_XEMPTY = B_XFULL + 1, B_DRAIN = B_XEMPTY + 1, B_XSFREE = B_DRAIN + 1,
                             B_XSFULL = B_XSFREE + 1, B_RFULL = B_XSFULL + 1,
                             B_REMPTY = B_RFULL + kRawNS, B_DRAIN2 = B_REMPTY + kRawNS,
-                            B_COUNT = B_DRAIN2 + 1;
+                            B_STALL = B_DRAIN2 + 1, B_COUNT = B_STALL + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;   // tmem slot, abort flag, ok flag
   static constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;  // + alignment slack
 };
@@ -133,6 +141,106 @@ static_assert(Cfg<MODE_BF16>::kSmemBytes <= 232448, "shared memory");
 static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
+
+// The reference max of the online softmax, moved lazily: the running max m
+// moves to the tile's row max Mt only when Mt exceeds it by more than 2^8, so
+// that P = 2^(s - m_use) <= 256 and O is rescaled rarely.
+struct RowRef {
+  float m_use, alpha;
+  bool resc, live;
+  __device__ __forceinline__ RowRef(float m, float Mt) {
+    const float m_new = fmaxf(m, Mt);
+    resc = m_new > m + 8.0f;
+    m_use = resc ? m_new : m;
+    alpha = resc ? exp2_approx(m - m_new) : 1.0f;
+    live = Mt != -INFINITY;
+  }
+};
+
+// State of one P-warp thread handed to the wide-tile path (local memory).
+struct WideIO {
+  uint32_t eo[32];  // in: this CTA's E of the row (fp16 pairs)
+  uint32_t ep[32];  // in: the peer's E of the row; out: P of the row (16-bit pairs)
+  float mt, m;      // in: m_own + m_peer, the running reference max
+  float m_use, alpha, rs;
+  int resc, js, jr;  // out: rescale flag; in/out: message counters
+};
+
+// P of one row of a wide tile, in the log domain. term k = (s_own - m_own) +
+// (s_peer - m_peer), where a narrow half gives log2(E) - kEShift and a wide
+// half the exact fp32 value of its follow-up messages. Each term is one sum
+// of two values and IEEE addition commutes, so both CTAs form the same term.
+// A thread's row lies in one follow-up part (rows 0-63, then 64-127): with
+// both halves' parts of that row resident it takes the row max, then P =
+// 2^(term + mt - m_use), reading the parts twice. Called by all four P warps
+// (they all take part in every wait and release); returns false when a wait
+// gave up. Kept out of line: it runs rarely and must not raise the register
+// demand of the common path.
+template <bool kOutF16>
+__device__ __noinline__ bool wide_tile_row(WideIO& io, bool own_wide, bool peer_wide, uint32_t xs, uint32_t xr,
+                                           int h, int pid, uint32_t bar_xsfull, uint32_t bar_xsfree,
+                                           uint32_t bar_xfull, uint32_t xempty_remote, uint32_t rank,
+                                           const Guard& guard) {
+  const int lane = h & 31;
+  const uint32_t prow = (uint32_t)(h & 63) * 256u;
+  auto side = [&](bool w, uint32_t base, const uint32_t* e, int k) -> float {
+    if (w) {
+      const float4 o = ld_shared_v4f(base + prow + ((((uint32_t)k >> 2) ^ (uint32_t)(h & 7)) << 4));
+      const int j = k & 3;
+      return j == 0 ? o.x : j == 1 ? o.y : j == 2 ? o.z : o.w;
+    }
+    const float2 f = unpack_f16x2(e[k >> 1]);
+    return log2_approx((k & 1) ? f.y : f.x) - kEShift;
+  };
+  auto term = [&](int k) { return side(own_wide, xs, io.eo, k) + side(peer_wide, xr, io.ep, k); };
+  io.rs = 0.f;
+  io.m_use = io.m;
+  io.alpha = 1.0f;
+  io.resc = 0;
+  for (int part2 = 0; part2 < 2; ++part2) {
+    const bool mine = (h >> 6) == part2;
+    if (own_wide && !warp_ok(wait(bar_xsfull, io.js & 1, guard))) return false;
+    if (peer_wide) {
+      if (pid == 0) mbar_arrive_expect_tx(bar_xfull, kXPart);
+      if (!warp_ok(wait_cluster(bar_xfull, io.jr & 1, guard))) return false;
+    }
+    uint32_t dep = 0u;
+    if (mine) {
+      float y = -INFINITY;
+#pragma unroll 1
+      for (int k = 0; k < 64; ++k) y = fmaxf(y, term(k));
+      const float Mt = (io.mt == -INFINITY || y == -INFINITY) ? -INFINITY : io.mt + y;
+      const RowRef r(io.m, Mt);
+      const float cw = r.live ? io.mt - r.m_use : 0.f;
+      float rs = 0.f;
+#pragma unroll 1
+      for (int u = 0; u < 32; ++u) {
+        const float a0 = r.live ? exp2_approx(term(2 * u) + cw) : 0.f;
+        const float a1 = r.live ? exp2_approx(term(2 * u + 1) + cw) : 0.f;
+        rs += a0 + a1;
+        io.ep[u] = kOutF16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+        dep |= io.ep[u];
+      }
+      io.rs = rs;
+      io.m_use = r.m_use;
+      io.alpha = r.alpha;
+      io.resc = r.resc ? 1 : 0;
+    }
+    if (own_wide) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_xsfree);
+      ++io.js;
+    }
+    if (peer_wide) {
+      // the relaxed arrive must follow this warp's loads from the receive
+      // buffer: every P value depends on them
+      dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
+      if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
+      ++io.jr;
+    }
+  }
+  return true;
+}
 
 __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -191,6 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     mbar_init(bar(C::B_XEMPTY), kPWarps);  // one arrive per peer P warp
     mbar_init(bar(C::B_DRAIN), 1);
     mbar_init(bar(C::B_DRAIN2), 1);
+    mbar_init(bar(C::B_STALL), 1);
     for (int s = 0; s < C::kRawNS; ++s) {
       mbar_init(bar(C::B_RFULL + s), 1);
       mbar_init(bar(C::B_REMPTY + s), kDequantWarps);
@@ -222,6 +331,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
   if (threadIdx.x == 0) {
     *ok_flag = header_matches(hdr, p, kTile, fp) ? 1u : 0u;
     if (!*ok_flag && rank == 0) atomicOr(p.status, STATUS_STALE);
+    if (*ok_flag && p.stall_cycles) {
+      // test hook: a bounded wait on a barrier nothing arrives at gives up
+      // and reports STATUS_TIMEOUT; nothing has been issued yet, so the CTA
+      // simply skips its work
+      const Guard g_stall{abort_flag, p.status, p.stall_cycles};
+      if (!wait(bar(C::B_STALL), 0, g_stall)) *ok_flag = 0u;
+    }
   }
   __syncthreads();
   const uint32_t tmem = *tmem_slot;
@@ -366,6 +482,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     Piece pc;
     int g = 0;
     bool failed = false;
+    // largest block scale seen: a scale of at most 146 (block amax <= 65408)
+    // keeps its fp16 copy at most 146 (an fp16 value), so no product code x
+    // scale (|code| <= 448) exceeds fp16's 65504
+    float sc_max = 0.f;
     while (!failed && it.next(pc)) {
       MaskStream<kSparse> ms;
       ms.start(p, pc);
@@ -393,6 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             // dense: 16 B per row; sparse: rows 4k..4k+3 share a 128-B unit
             const int srow = kSparse ? (row >> 2) * 32 + (row & 3) * 4 : row * 4;
             const float sc = scales[srow + 2 * rank + (unit >> 4)];
+            sc_max = fmaxf(sc_max, sc);
             // e4m3 -> f16 is exact; the product rounds once more through the
             // fp16 copy of the scale (both roundings are below 2^-11 relative)
             const uint32_t sc2 = pack_f16x2(sc, sc);
@@ -411,6 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
       }
     }
+    if (__any_sync(0xffffffffu, !(sc_max <= 146.0f)) && lane == 0) atomicOr(p.status, STATUS_RANGE);
   } else if (ok && lane == 0 && (warp == 1 || warp == C::kPvWarp)) {
     // ---------------- UMMA issue ----------------
     // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
@@ -531,9 +653,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
         }
         if constexpr (kFp8) {  // latent operands of FP8 caches are fp16
+          float qmax = 0.f;
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            r[k] = pack_f16x2_sat(__uint_as_float(r[k] << 16), __uint_as_float(r[k] & 0xFFFF0000u));
+          for (int k = 0; k < 64; ++k) {
+            const float x0 = __uint_as_float(r[k] << 16), x1 = __uint_as_float(r[k] & 0xFFFF0000u);
+            qmax = fmaxf(qmax, fmaxf(fabsf(x0), fabsf(x1)));
+            r[k] = pack_f16x2_sat(x0, x1);
+          }
+          // beyond fp16's largest finite value the query was saturated
+          if (qmax > 65504.f) atomicOr(p.status, STATUS_RANGE);
         }
         tc_fence_after();
         tmem_st32(tl + kColQ + 64u * half, r);
@@ -548,7 +676,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     PieceIter it(p, part);
     Piece pc;
     int g = 0, qi = 0;
+    int js = 0;  // messages this CTA has sent
     bool failed = false;
+    // XS may be (re)staged once this CTA's P warps have read message js-1 from
+    // it and the peer has read its copy (which frees the peer's receive buffer)
+    auto xs_free = [&]() {
+      return warp_ok(wait(bar(C::B_XSFREE), (js & 1) ^ 1, guard)) &&
+             warp_ok(wait_cluster(bar(C::B_XEMPTY), (js & 1) ^ 1, guard));
+    };
+    const uint32_t xs = sb + C::OFF_XS;
     while (!failed && it.next(pc)) {
       if (!load_q(pc, qi++)) break;
       MaskStream<kSparse> ms;
@@ -564,12 +700,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_SEMPTY));
-        // row max of the raw scores (the scale is positive, so it commutes
-        // with the max); masked tokens become -inf (their rows may hold NaN)
+        // row max and min of the raw scores over the valid tokens (the scale
+        // is positive, so it commutes with both); masked tokens become -inf
+        // (their rows may hold NaN)
+        float lo0 = INFINITY, lo1 = INFINITY;
         if (vm != ~0ull) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (!((vm >> k) & 1ull)) sr[k] = 0xFF800000u;  // -inf
+          for (int k = 0; k < 64; ++k) {
+            const bool v = (vm >> k) & 1ull;
+            if (k & 1) lo1 = v ? fminf(lo1, __uint_as_float(sr[k])) : lo1;
+            else lo0 = v ? fminf(lo0, __uint_as_float(sr[k])) : lo0;
+            if (!v) sr[k] = 0xFF800000u;  // -inf
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            lo0 = fminf(lo0, __uint_as_float(sr[k]));
+            lo1 = fminf(lo1, __uint_as_float(sr[k + 1]));
+          }
         }
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -578,20 +726,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           m1 = fmaxf(m1, __uint_as_float(sr[k + 1]));
         }
         const float m_own = fmaxf(m0, m1) * sl2;
-        const float nref = m_own == -INFINITY ? 0.f : -m_own;
+        // wide: some valid token lies more than kNarrow binades below this
+        // half's maximum, where its fp16 factor would lose precision (false
+        // when no token is valid: +inf < -inf)
+        const bool wide = fminf(lo0, lo1) * sl2 < m_own - kNarrow;
+        const float nref = m_own == -INFINITY ? 0.f : kEShift - m_own;
         uint32_t e[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u)
           e[u] = pack_f16x2(exp2_approx(fmaf(__uint_as_float(sr[2 * u]), sl2, nref)),
                             exp2_approx(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nref)));
-        // XS is free once this CTA's P warps have read tile g-1 from it and the
-        // peer has read its copy (which frees the peer's receive buffer too)
-        if (!warp_ok(wait(bar(C::B_XSFREE), (g & 1) ^ 1, guard)) ||
-            !warp_ok(wait_cluster(bar(C::B_XEMPTY), (g & 1) ^ 1, guard))) {
-          failed = true;
-          break;
-        }
-        const uint32_t xs = sb + C::OFF_XS;
+        if (!xs_free()) { failed = true; break; }
         const uint32_t xs_row = xs + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -599,10 +744,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         reinterpret_cast<float*>(smem + C::OFF_XS + kXM)[h] = m_own;
         if (h == 0) *reinterpret_cast<uint64_t*>(smem + C::OFF_XS + kXMask) = vm;
         fence_proxy_async_smem();
-        named_sync(kEBar, 128);
+        const bool any_wide = named_sync_or(kEBar, 128, wide);
         if (h == 0) {
+          *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_XS + kXFlag) = any_wide ? 1u : 0u;
+          fence_proxy_async_smem();
           bulk_copy_to_peer(xr_remote, xs, kXBytes, xfull_remote);
           mbar_arrive(bar(C::B_XSFULL));
+        }
+        ++js;
+        if (any_wide) {
+          // Wide tile (rare: a partial-score spread of more than kNarrow
+          // binades inside one tile): the exact partial scores s_r - m_r
+          // follow as fp32, rows 0-63 and then rows 64-127, so that P can be
+          // formed in the log domain whatever the spread.
+          const float nd = m_own == -INFINITY ? 0.f : -m_own;
+          for (int part2 = 0; part2 < 2 && !failed; ++part2) {
+            if (!xs_free()) { failed = true; break; }
+            if ((h >> 6) == part2) {
+              const uint32_t row = xs + (h & 63) * 256;
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                float d[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) d[j] = fmaf(__uint_as_float(sr[4 * u + j]), sl2, nd);
+                st_shared_v4(row + ((u ^ (h & 7)) << 4), __float_as_uint(d[0]), __float_as_uint(d[1]),
+                             __float_as_uint(d[2]), __float_as_uint(d[3]));
+              }
+            }
+            fence_proxy_async_smem();
+            named_sync(kEBar, 128);
+            if (h == 0) {
+              bulk_copy_to_peer(xr_remote, xs, kXPart, xfull_remote);
+              mbar_arrive(bar(C::B_XSFULL));
+            }
+            ++js;
+          }
+          if (failed) break;
         }
       }
     }
@@ -617,7 +794,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     PieceIter it(p, part);
     Piece pc;
     int g = 0, pcount = 0;
+    int js = 0, jr = 0;  // own messages read from XS, peer messages read from XR
     bool failed = false;
+    // Hand the receive buffer back to the peer. The arrive is relaxed, so it
+    // must not be performed before this warp's loads from the buffer have
+    // returned: its address depends on every loaded value (through a mask that
+    // is zero at run time, the rank being 0 or 1).
+    auto release_xr = [&](uint32_t dep) {
+      dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
+      if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
+    };
     while (!failed && it.next(pc)) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       float m = -INFINITY, l = 0.f;
@@ -625,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         // (1) this CTA's own E and m of tile g, staged by the E warps (always
         // before the peer's copy of the same tile lands, so read first)
         uint32_t ep[32], eo[32];
-        if (!warp_ok(wait(bar(C::B_XSFULL), g & 1, guard))) { failed = true; break; }
+        if (!warp_ok(wait(bar(C::B_XSFULL), js & 1, guard))) { failed = true; break; }
         const uint32_t xs_row = sb + C::OFF_XS + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -635,22 +821,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
         const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + kXM)[h];
         const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + kXMask);
+        const bool own_wide = *reinterpret_cast<const volatile uint32_t*>(smem + C::OFF_XS + kXFlag) != 0u;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_XSFREE));
-        // 16-bit caches: unpacked while the peer's message is still on its
-        // way; FP8 caches (128 registers a thread) unpack it as it is used
-        float fo[kFp8 ? 1 : 64];
+        ++js;
+        // a[k]: the product E_own E_peer of token k (linear, up to 2^(2 kEShift)),
+        // or for a wide tile (s_own - m_own) + (s_peer - m_peer) (log2 domain).
+        // 16-bit caches unpack their own E while the peer's message is on its
+        // way; FP8 caches (128 registers a thread) unpack it as it is used.
+        float a[64];
         if constexpr (!kFp8) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const float2 f = unpack_f16x2(eo[u]);
-            fo[2 * u] = f.x;
-            fo[2 * u + 1] = f.y;
+            a[2 * u] = f.x;
+            a[2 * u + 1] = f.y;
           }
         }
+        auto own_pair = [&](int u) {
+          if constexpr (kFp8) return unpack_f16x2(eo[u]);
+          else return make_float2(a[2 * u], a[2 * u + 1]);
+        };
         // (2) the peer's E and m of tile g
         if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
-        if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
+        if (!warp_ok(wait_cluster(bar(C::B_XFULL), jr & 1, guard))) { failed = true; break; }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
@@ -658,35 +852,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           ep[4 * u + 2] = __float_as_uint(o.z); ep[4 * u + 3] = __float_as_uint(o.w);
         }
         const float m_peer = xr_m[h];
+        const uint32_t peer_flag = *reinterpret_cast<const volatile uint32_t*>(smem + C::OFF_XR + kXFlag);
         {
-          // Hand the receive buffer back to the peer. The arrive is relaxed,
-          // so it must not be performed before this warp's loads from the
-          // buffer have returned: its address depends on every loaded value
-          // (through a mask that is zero at run time, the rank being 0 or 1).
-          uint32_t dep = __float_as_uint(m_peer);
+          uint32_t dep = __float_as_uint(m_peer) | peer_flag;
 #pragma unroll
           for (int u = 0; u < 8; ++u) dep |= ep[4 * u];
-          dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
-          if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
+          release_xr(dep);
         }
-        // (3) P with lazy rescale against the running reference max (P <= 256)
-        const float mt = m_own + m_peer;  // upper bound of the tile's scaled row max
-        const float m_new = fmaxf(m, mt);
-        const bool resc = m_new > m + 8.0f;
-        const float m_use = resc ? m_new : m;
-        const float alpha = resc ? exp2_approx(m - m_new) : 1.0f;
-        const float cf = mt == -INFINITY ? 0.f : exp2_approx(mt - (m_use == -INFINITY ? 0.f : m_use));
-        float rs0 = 0.f, rs1 = 0.f;
+        ++jr;
+        const bool peer_wide = peer_flag != 0u;
+        // (3) the tile's row max Mt relative to mt = m_own + m_peer (an upper
+        // bound of it, far above it when the halves peak on different
+        // tokens), then P = 2^(s - m_use) against the running reference max
+        const float mt = m_own + m_peer;
+        float m_use, alpha, rs0 = 0.f, rs1 = 0.f;
+        bool resc;
+        if (!(own_wide || peer_wide)) {  // the same in every thread of both CTAs
+          // both halves narrow: every valid factor is a normal fp16 value
+          // (relative error 2^-11) and the product is exact in fp32
+          float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float2 fq = unpack_f16x2(ep[u]);
-          const float2 fw = kFp8 ? unpack_f16x2(eo[u]) : make_float2(fo[(2 * u) % (kFp8 ? 1 : 64)],
-                                                                       fo[(2 * u + 1) % (kFp8 ? 1 : 64)]);
-          const float a0 = fw.x * fq.x * cf;
-          const float a1 = fw.y * fq.y * cf;
-          rs0 += a0;
-          rs1 += a1;
-          ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+          for (int u = 0; u < 32; ++u) {
+            const float2 fq = unpack_f16x2(ep[u]);
+            const float2 fw = own_pair(u);
+            a[2 * u] = fw.x * fq.x;
+            a[2 * u + 1] = fw.y * fq.y;
+            p0 = fmaxf(p0, a[2 * u]);
+            p1 = fmaxf(p1, a[2 * u + 1]);
+          }
+          const float pm = fmaxf(p0, p1);
+          const float Y = pm > 0.f ? log2_approx(pm) - 2.f * kEShift : -INFINITY;
+          const RowRef r(m, (mt == -INFINITY || Y == -INFINITY) ? -INFINITY : mt + Y);
+          m_use = r.m_use;
+          alpha = r.alpha;
+          resc = r.resc;
+          // P = a * 2^(mt - 2 kEShift - m_use)
+          const float cf = r.live ? exp2_approx((mt - m_use) - 2.f * kEShift) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float a0 = a[2 * u] * cf, a1 = a[2 * u + 1] * cf;
+            rs0 += a0;
+            rs1 += a1;
+            ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+          }
+        } else {
+          // a wide tile (a half whose valid scores spread over more than
+          // kNarrow binades): exact log-domain P, out of line
+          WideIO io;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            if constexpr (kFp8) io.eo[u] = eo[u];
+            else io.eo[u] = pack_f16x2(a[2 * u], a[2 * u + 1]);  // exact round trip
+            io.ep[u] = ep[u];
+          }
+          io.mt = mt;
+          io.m = m;
+          io.js = js;
+          io.jr = jr;
+          if (!wide_tile_row<kFp16 || kFp8>(io, own_wide, peer_wide, sb + C::OFF_XS, sb + C::OFF_XR, h, pid,
+                                             bar(C::B_XSFULL), bar(C::B_XSFREE), bar(C::B_XFULL), xempty_remote,
+                                             rank, guard)) {
+            failed = true;
+            break;
+          }
+          js = io.js;
+          jr = io.jr;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) ep[u] = io.ep[u];
+          m_use = io.m_use;
+          alpha = io.alpha;
+          resc = io.resc != 0;
+          rs0 = io.rs;
         }
         l = l * alpha + (rs0 + rs1);
         m = m_use;

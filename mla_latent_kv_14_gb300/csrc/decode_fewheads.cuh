@@ -57,7 +57,7 @@ constexpr uint32_t OFF_BAR = OFF_RED + kSoftWarps * kNH * 4;
 enum : uint32_t {
   B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
   B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2, B_OEMPTY = B_PEMPTY + 2,
-  B_DRAIN = B_OEMPTY + 1, B_COUNT = B_DRAIN + 1
+  B_DRAIN = B_OEMPTY + 1, B_STALL = B_DRAIN + 1, B_COUNT = B_STALL + 1
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;
@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_OEMPTY), kSoftWarps);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_STALL), 1);
     *abort_flag = 0u;
   }
   if (warp == 1) {
@@ -112,6 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
     if (!*ok_flag) atomicOr(p.status, STATUS_STALE);
     fence_mbar_init();
+    if (*ok_flag && p.stall_cycles) {
+      // test hook: a bounded wait on a barrier nothing arrives at gives up
+      // and reports STATUS_TIMEOUT before anything is issued
+      const Guard g_stall{abort_flag, p.status, p.stall_cycles};
+      if (!wait(bar(B_STALL), 0, g_stall)) *ok_flag = 0u;
+    }
   }
   tc_fence_before();
   __syncthreads();

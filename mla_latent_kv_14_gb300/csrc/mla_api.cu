@@ -92,6 +92,10 @@ bool make_map_4d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, const
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// test hook (mla_set_test_stall): cycles the next launches wait on a barrier
+// nothing arrives at before giving up; 0 in normal use
+std::atomic<uint32_t> g_test_stall{0};
+
 // per-device number of co-resident 2-CTA clusters of the 128-head decode
 // kernel, and of co-resident CTAs of the few-heads kernel
 std::atomic<int> g_parts[kMaxDevices];
@@ -159,6 +163,7 @@ const char* mla_status_string(int s) {
     case MLA_ERR_INDEX: return "out-of-range page or index skipped";
     case MLA_ERR_TIMEOUT: return "device pipeline wait timed out";
     case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_RANGE: return "a value beyond the fp16 range of the FP8 path was saturated";
     default: return "unknown status";
   }
 }
@@ -235,13 +240,15 @@ mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, in
 namespace {
 enum : int { STAGE_SPLIT = 1, STAGE_COMBINE = 2 };
 
-mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
-                       int page_block, const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens,
-                       int batch, int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
-                       int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
-                       void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  // ---- host-side argument checks (nothing is enqueued on failure) ----
-  if (!q || !kvcache || !out || !lse || !workspace || !metadata || !num_splits) return MLA_ERR_INVALID_ARG;
+// Host-side argument checks of a decode call; nothing is enqueued. The
+// workspace is checked only when the caller supplies one (check_ws).
+mla_status validate_decode(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks, int page_block,
+                           const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens, int batch,
+                           int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
+                           int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+                           void* out, float* lse, bool check_ws, void* workspace, size_t workspace_bytes) {
+  if (!q || !kvcache || !out || !lse || (check_ws && !workspace) || !metadata || !num_splits)
+    return MLA_ERR_INVALID_ARG;
   if (q_dtype != MLA_DTYPE_BF16 && q_dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
   if (head_dim_v != kDV || page_block != kTile) return MLA_ERR_INVALID_ARG;
   if (batch <= 0 || s_q <= 0 || parts <= 0 || num_blocks <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
@@ -249,9 +256,10 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   if (indices && causal) return MLA_ERR_INVALID_ARG;        // the index list already fixes the key set
   if ((indices != nullptr) != (topk > 0)) return MLA_ERR_INVALID_ARG;
   if (!indices && (!block_table || max_blocks <= 0 || !cache_seqlens)) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kvcache, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(lse, 4))
+  if (!aligned(q, 16) || !aligned(kvcache, 16) || !aligned(out, 16) || (check_ws && !aligned(workspace, 256)) ||
+      !aligned(lse, 4))
     return MLA_ERR_INVALID_ARG;
-  if (workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
+  if (check_ws && workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
   if (num_blocks * (int64_t)page_block >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
   if (h_q != 128 && h_q != kFewHeads) return MLA_ERR_UNSUPPORTED;
   if (h_q == kFewHeads && (indices || is_fp8)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
@@ -259,6 +267,21 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   if (is_fp8 && q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED; // FP8 rows pair with bf16 queries
   const int64_t qrows = (int64_t)batch * s_q * h_q;
   if (qrows >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
+                       int page_block, const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens,
+                       int batch, int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
+                       int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  // ---- host-side argument checks (nothing is enqueued on failure) ----
+  const mla_status v = validate_decode(q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks,
+                                       cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
+                                       softmax_scale, causal, is_fp8, indices, topk, out, lse, true, workspace,
+                                       workspace_bytes);
+  if (v != MLA_OK) return v;
+  const int64_t qrows = (int64_t)batch * s_q * h_q;
 
   int dev = 0;
   MLA_CUDA(cudaGetDevice(&dev));
@@ -334,6 +357,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.is_fp8 = is_fp8 ? 1 : 0;
   p.parts = parts;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.stall_cycles = g_test_stall.load(std::memory_order_relaxed);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the decode kernels wait for the preceding grid themselves (griddepcontrol),
@@ -435,8 +459,9 @@ mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* st
 }
 
 mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int tokens, int h_q, int dtype,
-                        void* stream) {
+                        uint32_t* status, void* stream) {
   if (tokens < 0 || h_q < 1 || (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16)) return MLA_ERR_INVALID_ARG;
+  if (status && !aligned(status, 4)) return MLA_ERR_INVALID_ARG;
   if (tokens == 0) return MLA_OK;
   if (!q_nope || !w_uk || !q_out || !aligned(q_nope, 16) || !aligned(w_uk, 16) || !aligned(q_out, 16))
     return MLA_ERR_INVALID_ARG;
@@ -450,23 +475,25 @@ mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int t
       !make_map_4d(&tm_b, w_uk, dt, {64, 128, 8, H}, {1024, 128, 128 * 1024}, {64, 128, 8, 1}))
     return MLA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t stall = g_test_stall.load(std::memory_order_relaxed);
   const dim3 grid((unsigned)h_q, (unsigned)((tokens + absorb::kTokTile - 1) / absorb::kTokTile));
   if (dtype == MLA_DTYPE_FP16) {
     MLA_CUDA(set_smem(absorb::mla_absorb_q_kernel<true>, absorb::kAbsorbSmem));
     absorb::mla_absorb_q_kernel<true><<<grid, absorb::kThreads, absorb::kAbsorbSmem, st>>>(tm_a, tm_b, q_out, tokens,
-                                                                                           h_q, nullptr);
+                                                                                           h_q, status, stall);
   } else {
     MLA_CUDA(set_smem(absorb::mla_absorb_q_kernel<false>, absorb::kAbsorbSmem));
     absorb::mla_absorb_q_kernel<false><<<grid, absorb::kThreads, absorb::kAbsorbSmem, st>>>(tm_a, tm_b, q_out, tokens,
-                                                                                            h_q, nullptr);
+                                                                                            h_q, status, stall);
   }
   MLA_CUDA(cudaGetLastError());
   return MLA_OK;
 }
 
 mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_out, int tokens, int h_q, int dtype,
-                          void* stream) {
+                          uint32_t* status, void* stream) {
   if (tokens < 0 || h_q < 1 || (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16)) return MLA_ERR_INVALID_ARG;
+  if (status && !aligned(status, 4)) return MLA_ERR_INVALID_ARG;
   if (tokens == 0) return MLA_OK;
   if (!o_lat || !w_uv || !o_out || !aligned(o_lat, 16) || !aligned(w_uv, 16) || !aligned(o_out, 16))
     return MLA_ERR_INVALID_ARG;
@@ -480,15 +507,16 @@ mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_out, int 
       !make_map_4d(&tm_b, w_uv, dt, {64, 128, 8, H}, {1024, 128, 128 * 1024}, {64, 128, 4, 1}))
     return MLA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t stall = g_test_stall.load(std::memory_order_relaxed);
   const dim3 grid((unsigned)h_q, (unsigned)((tokens + absorb::kTokTile - 1) / absorb::kTokTile));
   if (dtype == MLA_DTYPE_FP16) {
     MLA_CUDA(set_smem(absorb::mla_up_project_kernel<true>, absorb::kUpSmem));
     absorb::mla_up_project_kernel<true><<<grid, absorb::kThreads, absorb::kUpSmem, st>>>(tm_a, tm_b, o_out, tokens,
-                                                                                         h_q, nullptr);
+                                                                                         h_q, status, stall);
   } else {
     MLA_CUDA(set_smem(absorb::mla_up_project_kernel<false>, absorb::kUpSmem));
     absorb::mla_up_project_kernel<false><<<grid, absorb::kThreads, absorb::kUpSmem, st>>>(tm_a, tm_b, o_out, tokens,
-                                                                                          h_q, nullptr);
+                                                                                          h_q, status, stall);
   }
   MLA_CUDA(cudaGetLastError());
   return MLA_OK;
@@ -506,8 +534,11 @@ mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits) {
   if (v & STATUS_TIMEOUT) return MLA_ERR_TIMEOUT;
   if (v & STATUS_STALE) return MLA_ERR_STALE_METADATA;
   if (v & STATUS_INDEX) return MLA_ERR_INDEX;
+  if (v & STATUS_RANGE) return MLA_ERR_RANGE;
   return MLA_OK;
 }
+
+void mla_set_test_stall(uint32_t cycles) { g_test_stall.store(cycles, std::memory_order_relaxed); }
 
 }  // extern "C"
 
@@ -529,22 +560,28 @@ namespace {
 constexpr size_t kStaticWsBytes = size_t(32) << 20;  // 32 MiB per device
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
-std::once_flag g_static_once[kMaxDevices];
-void* g_static_ptr[kMaxDevices];
-cudaError_t g_static_err[kMaxDevices];
+std::mutex g_static_mu[kMaxDevices];
+std::atomic<void*> g_static_ptr[kMaxDevices];
 
 // Host code may not use g_static_ws directly (its name is a host-side stand-in,
-// not a device address): look the device address up once per device, with
-// that device current.
+// not a device address): look the device address up with that device current,
+// and keep it once the lookup has succeeded. A failed lookup (for example one
+// made during a stream capture) is not remembered: the next call tries again.
 void* static_ws_ptr(int dev, cudaError_t* err) {
-  std::call_once(g_static_once[dev], [&] {
-    void* ptr = nullptr;
-    g_static_err[dev] = cudaGetSymbolAddress(&ptr, g_static_ws);
-    g_static_ptr[dev] = g_static_err[dev] == cudaSuccess ? ptr : nullptr;
+  *err = cudaSuccess;
+  void* ptr = g_static_ptr[dev].load(std::memory_order_acquire);
+  if (ptr) return ptr;
+  std::lock_guard<std::mutex> lock(g_static_mu[dev]);
+  ptr = g_static_ptr[dev].load(std::memory_order_relaxed);
+  if (ptr) return ptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_ws);
+  if (e != cudaSuccess || !ptr) {
     (void)cudaGetLastError();
-  });
-  *err = g_static_err[dev];
-  return g_static_ptr[dev];
+    *err = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    return nullptr;
+  }
+  g_static_ptr[dev].store(ptr, std::memory_order_release);
+  return ptr;
 }
 }  // namespace
 
@@ -557,6 +594,12 @@ extern "C" mla_status mla_decode_with_kvcache_noalloc(
   if (need == 0) return MLA_ERR_INVALID_ARG;
   if (need > kStaticWsBytes) return MLA_ERR_INVALID_ARG;  // beyond the fixed scratch: use mla_decode_with_kvcache
   if (status && !aligned(status, 4)) return MLA_ERR_INVALID_ARG;
+  // every argument check happens before the first enqueue (the status
+  // memset); the fixed array is the workspace, sized and aligned above
+  const mla_status v = validate_decode(q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks,
+                                       cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
+                                       softmax_scale, causal, is_fp8, indices, topk, out, lse, false, nullptr, 0);
+  if (v != MLA_OK) return v;
   int dev = 0;
   MLA_CUDA(cudaGetDevice(&dev));
   if (dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;

@@ -66,6 +66,10 @@ struct DecodeParams {
   int batch, s_q, h_q, topk, causal, is_fp8, parts;
   int out_v8;                  // out is 32-B aligned: 32-byte stores in the epilogue
   float scale_log2;            // softmax_scale * log2(e)
+  // test hook, 0 in normal use: before any copy is issued, thread 0 of each CTA
+  // waits this many cycles on a barrier that nothing arrives at, so the wait
+  // gives up, reports STATUS_TIMEOUT and the CTA skips all work
+  uint32_t stall_cycles;
 };
 
 struct CombineParams {

@@ -13,6 +13,7 @@ namespace mla {
 constexpr uint32_t STATUS_INDEX = 1u;    // out-of-range page / index skipped
 constexpr uint32_t STATUS_TIMEOUT = 2u;  // a pipeline wait gave up
 constexpr uint32_t STATUS_STALE = 4u;    // metadata does not match the call
+constexpr uint32_t STATUS_RANGE = 8u;    // FP8 path: a value beyond fp16 range was saturated
 
 // ---------------------------------------------------------------------------
 // addresses, timers
@@ -380,6 +381,12 @@ MLA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MLA_DEV float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+MLA_DEV float log2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 

@@ -8,6 +8,6 @@ from .mla_oracle import (  # noqa: F401
     E4M3_MAX, FP8_ROW_BYTES,
     e4m3_value_table, e4m3_encode_rne,
     quantize_kv_fp8, dequantize_kv_fp8,
-    attend, visible_rows, mla_decode, mla_decode_sampled, absorb_q, up_project,
+    attend, visible_rows, mla_decode, absorb_q, up_project,
     bf16_to_f64, to_f64,
 )

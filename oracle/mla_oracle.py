@@ -39,7 +39,7 @@ brute force, torch's float8 cast, an integer rounding model).
 from __future__ import annotations
 
 import math
-from typing import Iterable, Optional, Sequence, Tuple
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -271,27 +271,3 @@ def mla_decode(q, kv_rows, *, cache_seqlens=None, block_table=None, page_block: 
             o, ls = attend(q[b, i, hsel], kv_rows[rows], softmax_scale, d_v)
             out[b, i], lse[b, i] = o, ls
     return out, lse, any_bad
-
-
-def mla_decode_sampled(q, kv_rows_fn, samples: Iterable[Tuple[int, int]], *, cache_seqlens=None,
-                       block_table=None, page_block: int = 64, softmax_scale: Optional[float] = None,
-                       causal: bool = False, indices=None, num_rows: Optional[int] = None,
-                       d_v: int = _LAT):
-    """The same definition for a few (b, i) query positions of a large problem.
-
-    ``kv_rows_fn(rows)`` returns float64 [len(rows), d_k] for absolute row
-    indices, so the whole cache never has to be converted. Returns a dict
-    (b, i) -> (out [h, d_v], lse [h]).
-    """
-    q = np.asarray(q, dtype=np.float64)
-    s_q = q.shape[1]
-    d_k = q.shape[3]
-    if softmax_scale is None:
-        softmax_scale = d_k ** -0.5
-    res = {}
-    for (b, i) in samples:
-        rows, _ = visible_rows(b, i, seqlens=cache_seqlens, block_table=block_table,
-                               page_block=page_block, s_q=s_q, causal=causal,
-                               indices=indices, num_rows=num_rows)
-        res[(b, i)] = attend(q[b, i], kv_rows_fn(rows), softmax_scale, d_v)
-    return res

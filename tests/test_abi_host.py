@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for must in ["mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits", "mla_quantize_kv_fp8", "mla_read_status",
                  "mla_absorb_q", "mla_up_project", "mla_decode_with_kvcache_noalloc",
-                 "mla_metadata_size", "mla_workspace_size", "mla_num_sm_parts", "mla_status_string"]:
+                 "mla_metadata_size", "mla_workspace_size", "mla_num_sm_parts", "mla_status_string",
+                 "mla_set_test_stall"]:
         assert must in names
 
 
@@ -45,8 +46,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert lib.mla_status_string(code)
+        assert b"unknown" not in lib.mla_status_string(code)
     assert b"unknown" in lib.mla_status_string(99)
 
 
@@ -112,13 +114,47 @@ def test_absorption_argument_checks(lib, name):
     device call; tokens = 0 is a no-op."""
     f = getattr(lib, name)
     mis = ctypes.c_void_p((1 << 20) + 8)
-    assert f(FAKE, FAKE, FAKE, -1, 128, 0, None) == 1          # negative token count
-    assert f(FAKE, FAKE, FAKE, 4, 0, 0, None) == 1             # no heads
-    assert f(FAKE, FAKE, FAKE, 4, 128, 7, None) == 1           # unknown dtype
-    assert f(None, FAKE, FAKE, 4, 128, 0, None) == 1           # null input
-    assert f(FAKE, None, FAKE, 4, 128, 0, None) == 1           # null weights
-    assert f(FAKE, FAKE, None, 4, 128, 0, None) == 1           # null output
-    assert f(mis, FAKE, FAKE, 4, 128, 0, None) == 1            # misaligned input
-    assert f(FAKE, mis, FAKE, 4, 128, 1, None) == 1            # misaligned weights
-    assert f(FAKE, FAKE, mis, 4, 128, 0, None) == 1            # misaligned output
-    assert f(None, None, None, 0, 128, 0, None) == 0           # nothing to do
+    assert f(FAKE, FAKE, FAKE, -1, 128, 0, None, None) == 1          # negative token count
+    assert f(FAKE, FAKE, FAKE, 4, 0, 0, None, None) == 1             # no heads
+    assert f(FAKE, FAKE, FAKE, 4, 128, 7, None, None) == 1           # unknown dtype
+    assert f(None, FAKE, FAKE, 4, 128, 0, None, None) == 1           # null input
+    assert f(FAKE, None, FAKE, 4, 128, 0, None, None) == 1           # null weights
+    assert f(FAKE, FAKE, None, 4, 128, 0, None, None) == 1           # null output
+    assert f(mis, FAKE, FAKE, 4, 128, 0, None, None) == 1            # misaligned input
+    assert f(FAKE, mis, FAKE, 4, 128, 1, None, None) == 1            # misaligned weights
+    assert f(FAKE, FAKE, mis, 4, 128, 0, None, None) == 1            # misaligned output
+    assert f(FAKE, FAKE, FAKE, 4, 128, 0, ctypes.c_void_p((1 << 20) + 2), None) == 1  # misaligned status word
+    assert f(None, None, None, 0, 128, 0, None, None) == 0           # nothing to do
+
+
+def _noalloc(lib, **kw):
+    a = dict(q=FAKE, q_dtype=0, kv=FAKE, num_blocks=8, page_block=64, bt=FAKE, max_blocks=8, sl=FAKE, batch=2,
+             s_q=1, h_q=128, dv=512, meta=FAKE, ns=FAKE, parts=4, scale=576 ** -0.5, causal=0, fp8=0, idx=None,
+             topk=0, out=FAKE, lse=FAKE, status=None, stream=None)
+    a.update(kw)
+    return lib.mla_decode_with_kvcache_noalloc(
+        a["q"], a["q_dtype"], a["kv"], a["num_blocks"], a["page_block"], a["bt"], a["max_blocks"], a["sl"],
+        a["batch"], a["s_q"], a["h_q"], a["dv"], a["meta"], a["ns"], a["parts"], a["scale"], a["causal"], a["fp8"],
+        a["idx"], a["topk"], a["out"], a["lse"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=256), 1),
+    (dict(q=None), 1),
+    (dict(idx=FAKE, topk=2048, causal=1), 1),
+    (dict(bt=None), 1),
+    (dict(q=ctypes.c_void_p((1 << 20) + 2)), 1),
+    (dict(status=ctypes.c_void_p((1 << 20) + 2)), 1),   # misaligned status word
+    (dict(batch=4096, parts=76), 1),                    # scratch beyond the fixed array
+    (dict(h_q=64), 2),
+])
+def test_noalloc_rejects_before_any_device_call(lib, kw, code):
+    """Every argument check of the allocation-free entry point runs before it
+    touches the device: on a host without a GPU any CUDA call would fail with
+    MLA_ERR_CUDA (6), so the argument error must come back instead."""
+    assert _noalloc(lib, **kw) == code
+
+
+def test_set_test_stall_is_host_only(lib):
+    lib.mla_set_test_stall(1000)
+    lib.mla_set_test_stall(0)

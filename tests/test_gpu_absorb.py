@@ -62,9 +62,9 @@ def test_empty_and_bad_args():
     mla.mla_absorb_q(case.q_nope[:0].to(DEV), case.w_uk.to(DEV), q_out)   # tokens = 0: nothing to do
     lib = mla.load_library()
     w = case.w_uk.to(DEV)
-    assert lib.mla_absorb_q(w.data_ptr(), w.data_ptr(), w.data_ptr(), -1, 2, 0, None) == 1
-    assert lib.mla_up_project(w.data_ptr(), w.data_ptr(), w.data_ptr(), 4, 2, 5, None) == 1
-    assert lib.mla_up_project(w.data_ptr() + 2, w.data_ptr(), w.data_ptr(), 4, 2, 0, None) == 1
+    assert lib.mla_absorb_q(w.data_ptr(), w.data_ptr(), w.data_ptr(), -1, 2, 0, None, None) == 1
+    assert lib.mla_up_project(w.data_ptr(), w.data_ptr(), w.data_ptr(), 4, 2, 5, None, None) == 1
+    assert lib.mla_up_project(w.data_ptr() + 2, w.data_ptr(), w.data_ptr(), 4, 2, 0, None, None) == 1
 
 
 def test_absorbed_chain_equals_naive_per_head_attention():

@@ -157,10 +157,13 @@ def test_fp16_cache():
 
 
 def test_gather_exact_single_dominant_key():
-    """One key with a score margin > 200 -> p = 1 exactly in fp32, so the
-    output equals that key's value row after the bf16 round trip. The margin
-    sits in two RoPE dims (512+b and 544+b), so the key dominates every partial
-    sum the kernel forms over a subset of the 576 dims."""
+    """One key with a score margin of about 200 log2 units -> p = 1 and every
+    other p = 0 in fp32, so the output equals that key's value row after the
+    bf16 round trip. The margin sits in two RoPE dims (512+b and 544+b), so the
+    key dominates every partial sum the kernel forms over a subset of the 576
+    dims, and the scores stay near 200, where fp32 holds them to 2^-16 (a far
+    larger margin would make the fp32 score itself inexact by more than the
+    bf16 rounding of p tolerates)."""
     case = synth.make_dense_case([200, 130], seed=11)
     sl = case.cache_seqlens.numpy()
     bt = case.block_table.numpy()
@@ -169,12 +172,12 @@ def test_gather_exact_single_dominant_key():
         q = case.q[b, 0].float()
         kvr = case.kv_rows[row].float().clone()
         kvr[512:] = 0
-        kvr[512 + b] = 100.0                       # only this key has large RoPE entries
-        kvr[544 + b] = 100.0
+        kvr[512 + b] = 26.0                        # only this key has large RoPE entries
+        kvr[544 + b] = 26.0
         case.kv_rows[row] = kvr.to(torch.bfloat16)
         qq = q.clone()
-        qq[:, 512 + b] = 100.0 * 24 * 4            # score margin >> 200 after the 1/24 scale
-        qq[:, 544 + b] = 100.0 * 24 * 4
+        qq[:, 512 + b] = 64.0                      # 64 * 26 / 24 * log2(e) = 100 log2 units per dim
+        qq[:, 544 + b] = 64.0
         case.q[b, 0] = qq.to(torch.bfloat16)
     out, lse, _ = run_dense(case)
     for b, tok in [(0, 137), (1, 64)]:
