@@ -57,6 +57,8 @@ WORKLOADS = {
 }
 SPARSE_TOKENS = 131072
 DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"
+L2_BYTES = 129e6       # GB300 L2; a workload whose touched bytes per step are below
+                       # twice this rotates several index sets between steps
 
 
 def load_peaks():
@@ -228,20 +230,24 @@ def torch_dtype(name):
     return getattr(torch, name)
 
 
-def oracle_rate(case, seqlens, budget_s, max_requests=None):
-    """The float64 oracle on whole requests (all heads) until the time budget
-    is used; returns (flops/s, description, requests done)."""
-    import numpy as np
+def oracle_rate(case, seqlens, budget_s, max_requests=None, raw=None):
+    """The float64 oracle on whole requests (all heads, every query position)
+    until the time budget is used. With `raw` (the FP8 rows, on any device)
+    each request's rows are dequantised by the oracle first, inside the timed
+    work. Returns (flops/s, description, requests done, seconds, busy cores)."""
     import oracle
     import synth
     s_q, causal = case.s_q, case.causal
     bt = case.block_table.numpy()
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     done_flops, done = 0.0, 0
     nreq = len(seqlens) if max_requests is None else min(max_requests, len(seqlens))
     for b in range(nreq):
         rows = synth.paged_rows_index(bt[b], seqlens[b], case.page_block)
-        kv = oracle.to_f64(case.kv_rows[torch_index(rows, case.kv_rows.device)].cpu())
+        if raw is not None:
+            kv = oracle.dequantize_kv_fp8(raw[torch_index(rows, raw.device)].cpu().numpy())
+        else:
+            kv = oracle.to_f64(case.kv_rows[torch_index(rows, case.kv_rows.device)].cpu())
         q = oracle.to_f64(case.q[b].cpu())
         for i in range(s_q):
             L = seqlens[b] - (s_q - 1 - i if causal else 0)
@@ -250,8 +256,38 @@ def oracle_rate(case, seqlens, budget_s, max_requests=None):
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    dt = time.perf_counter() - t0
-    return done_flops / dt, f"{done} of {len(seqlens)} requests (all {case.h_q} heads, s_q={s_q})", done, dt
+    dt, cpu = time.perf_counter() - t0, time.process_time() - c0
+    what = "dequantised FP8 " if raw is not None else ""
+    return (done_flops / dt, f"{done} of {len(seqlens)} requests ({what}all {case.h_q} heads, s_q={s_q})", done, dt,
+            cpu / dt)
+
+
+def oracle_rate_sparse(q, raw, indices, scale, budget_s):
+    """The float64 oracle on whole sparse queries: gather the query's rows by
+    index, dequantise them, attend; until the time budget is used."""
+    import numpy as np
+    import oracle
+    B, s_q = indices.shape[0], indices.shape[1]
+    t0, c0 = time.perf_counter(), time.process_time()
+    done_flops, done = 0.0, 0
+    for n in range(B * s_q):
+        b, i = n // s_q, n % s_q
+        sel = indices[b, i]
+        sel = sel[sel >= 0]
+        kv = oracle.dequantize_kv_fp8(raw[torch_index(sel.astype(np.int64), raw.device)].cpu().numpy())
+        oracle.attend(oracle.to_f64(q[b, i].cpu()), kv, scale)
+        done_flops += 2.0 * q.shape[2] * 1088 * len(sel)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt, cpu = time.perf_counter() - t0, time.process_time() - c0
+    return (done_flops / dt, f"{done} of {B * s_q} queries (index gather + dequantise + attend, all {q.shape[2]} heads)",
+            done, dt, cpu / dt)
+
+
+def cpu_baseline_line(rate, desc, busy):
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "cores_busy": round(busy, 1),
+            "kind": "oracle", "sample": f"float64 oracle on {desc} of this workload"}
 
 
 def torch_index(rows, device):
@@ -271,12 +307,25 @@ def run_ours(args, w, rank, world, device):
     is_fp8 = kind in ("fp8", "sparse")
     q = case.q
     bt = sl = idx = None
+    idx_sets = [None]
     if kind == "sparse":
+        import synth
         raw = mla.mla_quantize_kv_fp8(case.kv_rows)          # the FP8 cache, written by the library
         case.kv_rows = None
         kv = raw.view(-1, 64, 1, 656)
-        idx = case.indices.to(device)
-        flops, algo_bytes, kv_bytes = work_counts(None, s_q, False, row_bytes=656, indices=case.indices.numpy())
+        # the rows one step touches may fit in L2 (topk 2048: about 50 MB per
+        # query position); then several seeded index sets are rotated so that
+        # more than twice the L2 passes between two uses of one set
+        sets = [case.indices.numpy()]
+        counts = [work_counts(None, s_q, False, row_bytes=656, indices=sets[0])]
+        n_sets = max(1, math.ceil(2 * L2_BYTES / counts[0][2]))
+        for k in range(1, n_sets):
+            sets.append(synth.make_sparse_case(w["batch"], s_q, w["topk"], tokens_per_request=SPARSE_TOKENS,
+                                               seed=1000 + k, with_rows=False).indices.numpy())
+            counts.append(work_counts(None, s_q, False, row_bytes=656, indices=sets[-1]))
+        flops, algo_bytes, kv_bytes = (statistics.mean(c[j] for c in counts) for j in range(3))
+        idx_sets = [torch.from_numpy(x).to(device) for x in sets]
+        idx = idx_sets[0]
         meta_args = dict(batch=q.shape[0], topk=idx.shape[-1], is_fp8=True, device=device)
     else:
         bt = case.block_table.to(device)
@@ -292,20 +341,22 @@ def run_ours(args, w, rank, world, device):
     lse = torch.empty(q.shape[0], s_q, h_q, dtype=torch.float32, device=device)
     meta, ns = mla.mla_get_metadata(sl, s_q, h_q, **meta_args)
     stream = torch.cuda.current_stream(device)
-    dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8, indices=idx)
+    dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8)
 
-    def step():
+    def step(k=0):
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
-        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
+        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=idx_sets[k % len(idx_sets)],
+                                    **dec_kw)
 
     # correctness gate before timing: device status must be clean
-    step()
+    for k in range(len(idx_sets)):
+        step(k)
     st, bits = mla.mla_read_status(device=device)
     if st != 0:
         raise RuntimeError(f"device status {st} (bits {bits}) before timing")
 
-    for _ in range(args.warmup):
-        step()
+    for k in range(args.warmup):
+        step(k)
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
@@ -314,8 +365,8 @@ def run_ours(args, w, rank, world, device):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for k in range(args.steps):
+            step(k)
         e1.record(stream)
         torch.cuda.synchronize(device)
     elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
@@ -331,9 +382,10 @@ def run_ours(args, w, rank, world, device):
         ev[k][0].record(stream)
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
         ev[k][1].record(stream)
-        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
+        ik = idx_sets[k % len(idx_sets)]
+        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
         ev[k][2].record(stream)
-        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, out=out, lse=lse, **dec_kw)
+        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
         ev[k][3].record(stream)
     torch.cuda.synchronize(device)
     t_meta = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
@@ -351,6 +403,7 @@ def run_ours(args, w, rank, world, device):
     if not args.no_e2e:
         nbuf = 2
         host_in = [q.cpu().pin_memory()] + [t.cpu().pin_memory() for t in (bt, sl, idx) if t is not None]
+        host_idx = [t.cpu().pin_memory() for t in idx_sets] if idx is not None else None
         dev_in = [[torch.empty_like(h, device=device) for h in host_in] for _ in range(nbuf)]
         outs = [torch.empty_like(out) for _ in range(nbuf)]
         lses = [torch.empty_like(lse) for _ in range(nbuf)]
@@ -365,7 +418,10 @@ def run_ours(args, w, rank, world, device):
             j = k % nbuf
             with torch.cuda.stream(s_in):
                 s_in.wait_event(ev_comp[j])          # the compute that last read buffer j is done
-                for hsrc, ddst in zip(host_in, dev_in[j]):
+                srcs = list(host_in)
+                if host_idx is not None:             # the index set of this step (rotated as above)
+                    srcs[-1] = host_idx[k % len(host_idx)]
+                for hsrc, ddst in zip(srcs, dev_in[j]):
                     ddst.copy_(hsrc, non_blocking=True)
                 ev_in[j].record(s_in)
             stream.wait_event(ev_in[j])
@@ -400,7 +456,8 @@ def run_ours(args, w, rank, world, device):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(t_e2e * 1e3, 4), "pipelined_buffers": nbuf}
     return dict(elapsed=elapsed, flops=flops, algo_bytes=algo_bytes, kv_bytes=kv_bytes, t_meta=t_meta, t_dec=t_dec,
-                t_comb=t_comb, clocks=clk.summary(), e2e=e2e, parts=meta.parts, case=case, seqlens=seqlens)
+                t_comb=t_comb, clocks=clk.summary(), e2e=e2e, parts=meta.parts, case=case, seqlens=seqlens,
+                raw=raw if is_fp8 else None, n_sets=len(idx_sets))
 
 
 def run_absorb(args, w, world, device, hbm_peak, tc_peak, peak_src):
@@ -455,6 +512,19 @@ def run_absorb(args, w, world, device, hbm_peak, tc_peak, peak_src):
     t_e2e = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, device)
     achieved = algo_bytes / t_step / 1e9
     bound = "hbm" if algo_bytes / (hbm_peak * 1e9) >= flops / (tc_peak * 1e12) else "tensor"
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        # the oracle's two per-head products, token by token, until the budget is used
+        import oracle
+        qc, ol = oracle.to_f64(case.q_nope.cpu()), oracle.to_f64(case.o_lat.cpu())
+        wuk, wuv = oracle.to_f64(case.w_uk.cpu()), oracle.to_f64(case.w_uv.cpu())
+        t0, c0, toks = time.perf_counter(), time.process_time(), 0
+        while toks < T and time.perf_counter() - t0 < args.cpu_budget:
+            oracle.absorb_q(qc[toks:toks + 1], wuk)
+            oracle.up_project(ol[toks:toks + 1], wuv)
+            toks += 1
+        dt, busy = time.perf_counter() - t0, (time.process_time() - c0) / max(time.perf_counter() - t0, 1e-9)
+        cpu = cpu_baseline_line(2 * 2.0 * toks * h * 128 * 512 / dt, f"{toks} of {T} tokens (all {h} heads)", busy)
     return {
         "metric": "absorption GEMMs (q~ = W^UK^T q^C, o = W^UV o~) throughput", "impl": "ours",
         "value": round(whole_job_rate(flops, world, t_step) / 1e12, 3), "unit": "TFLOPS", "n_gpus": world,
@@ -466,7 +536,7 @@ def run_absorb(args, w, world, device, hbm_peak, tc_peak, peak_src):
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": None,
                      "kernel": "mla_absorb_q_kernel + mla_up_project_kernel", "peak_source": f"{peak_src} hbm_gbs"},
-        "cpu_baseline": None,
+        "cpu_baseline": cpu,
         "e2e": {"value": round(whole_job_rate(flops, world, t_e2e) / 1e12, 3), "unit": "TFLOPS",
                 "h2d_bytes_per_step": int(hq.numel() * 2 + ho.numel() * 2),
                 "d2h_bytes_per_step": int(hq_out.numel() * 2 + h_o.numel() * 2), "ms_per_step": round(t_e2e * 1e3, 4)},
@@ -534,11 +604,14 @@ def main():
                 "frac": round(achieved / tc_peak, 4), "traffic": stored_traffic(args.workload),
                 "kernel": kname, "peak_source": f"{peak_src} bf16_tflops"}
     cpu = None
-    if not args.no_cpu_baseline and world == 1 and w["kind"] == "dense":
-        cpu_case = r["case"]
-        rate, desc, _, _ = oracle_rate(cpu_case, r["seqlens"], args.cpu_budget)
-        cpu = {"value": round(rate / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"float64 oracle on {desc} of this workload"}
+    if not args.no_cpu_baseline and world == 1:
+        c = r["case"]
+        if w["kind"] == "sparse":
+            rate, desc, _, _, busy = oracle_rate_sparse(c.q, r["raw"], c.indices.numpy(), c.softmax_scale,
+                                                        args.cpu_budget)
+        else:
+            rate, desc, _, _, busy = oracle_rate(c, r["seqlens"], args.cpu_budget, raw=r["raw"])
+        cpu = cpu_baseline_line(rate, desc, busy)
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
@@ -552,7 +625,10 @@ def main():
                                else f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
                                else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),
                    "parallelism": f"replicas x{world}", "num_sm_parts": r["parts"],
-                   "l2": "inputs larger than L2 (KV cache %.0f MB per replica)" % (r["kv_bytes"] / 1e6)},
+                   "l2": ("inputs larger than L2 (KV cache %.0f MB per replica)" % (r["kv_bytes"] / 1e6)
+                          if r["n_sets"] == 1 else
+                          "inputs larger than L2: %d index sets rotated, %.0f MB of rows each"
+                          % (r["n_sets"], r["kv_bytes"] / 1e6))},
         "kv_gbs": round(kv_gbs, 1), "algo_gbs": round(world * r["algo_bytes"] / t_step / 1e9, 1),
         "roofline_time_frac": round(t_roof / t_step, 4),
         "kernel_us": {"metadata": round(r["t_meta"] * 1e6, 2), "decode": round(r["t_dec"] * 1e6, 2),
@@ -614,17 +690,18 @@ def run_reference(args, w, rank, world):
         sample = f"float64 oracle, one request of {L} tokens x {heads} heads per step (s_q position 0)"
     for _ in range(args.warmup):
         run()
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     for _ in range(args.steps):
         run()
+    busy = (time.process_time() - c0) / max(time.perf_counter() - t0, 1e-9)
     dt = (time.perf_counter() - t0) / args.steps
     val = flops / dt / 1e12
     line = {"impl": "reference", "metric": metric, "value": round(val, 6), "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": w.get("h_q", 128)},
-            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
+                             "cores_busy": round(busy, 1), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -104,7 +104,8 @@ MLA_API mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int
                             int topk, int is_fp8, int causal, int page_block, int num_sm_parts,
                             void* metadata, int32_t* num_splits, void* stream);
 
-/* Bytes of decode workspace (status word + fp32 split partials). */
+/* Bytes of decode workspace (status word, fp32 split partials, and one bit per
+ * (query position, head) row for the exact recompute). */
 MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts);
 
 /*
@@ -130,8 +131,11 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  *              and flagged as MLA_ERR_INDEX ("拆解" page, §八 sparse indices).
  * out          (device) [batch, s_q, h_q, 512] of q_dtype, written.
  * lse          (device) fp32 [batch, s_q, h_q], natural log, written.
- * workspace    (device) mla_workspace_size() bytes, 256-B aligned; its status
- *              word must be zeroed once before first use (mla_read_status clears it).
+ * workspace    (device) mla_workspace_size() bytes, 256-B aligned, zeroed once
+ *              before first use: it holds the status word (mla_read_status
+ *              clears it), the fp32 partials of cut requests and one bit per
+ *              (query position, head) row that the combine recomputes exactly
+ *              (the library leaves those bits zero after every call).
  * A request with no visible token gets out = 0 and lse = -inf.
  * FP8 caches (is_fp8 = 1) run the latent product in fp16: the bf16 query is
  * rounded to fp16 and each cache value is formed as fp16(code) x fp16(block
@@ -141,6 +145,14 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * instead. Out of range -- a query entry beyond 65504 in magnitude (saturated
  * to +-65504) or a block scale above 146 (block amax above 65408) -- the
  * status word records MLA_ERR_RANGE.
+ * Every cache type splits the 576 dims of a score between the two CTAs of a
+ * pair, which exchange fp16 factors 2^(partial score - partial max). The
+ * result is certified exact (to fp16 precision) for a row of a 64-token tile
+ * unless the two partial scores of its tokens disagree by more than about 22
+ * binades; such a row is recomputed exactly from q and the cache rows for
+ * 16-bit caches (by the combine step, so mla_decode_splitkv alone leaves it
+ * uncorrected until mla_combine_splits runs), and reported as MLA_ERR_RANGE
+ * for FP8 caches.
  * h_q = 128 with any cache; h_q = 16 with a dense 16-bit cache only: the few
  * heads fill the MMA's N dimension and the 64 tokens of a tile its M
  * dimension, the transposed formulation S^T = K Q^T, O^T = V^T P^T of the

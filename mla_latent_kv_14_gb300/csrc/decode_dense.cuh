@@ -17,12 +17,18 @@
 // the latent dims [256r, 256r+256) and the RoPE dims [512+32r, 544+32r).
 // Each CTA computes a partial score S_r over its dims with single-CTA UMMA
 // (M=128 heads, N=64 tokens). Instead of exchanging S_r, each CTA exponentiates
-// it, E_r = exp2((S_r - m_r) * scale*log2e) with m_r its partial row max, and
-// sends E_r (in [0,1]) as fp16 plus m_r: exp(S_0 + S_1 - m) = E_0 * E_1 *
-// exp(m_0 + m_1 - m) is exact algebra, so both CTAs form the same P = E_0 *
-// E_1 * 2^(m_0 + m_1 - m_ref) (identical fp16 operands, commutative products;
-// a factor below 2^-24 flushes to 0) and accumulate P . V
-// for their own half of the latent (M=128, N=256, K=64). No tensor-core work is
+// it, E_r = exp2((S_r - m_r) * scale*log2e + 15) with m_r its partial row max,
+// and sends E_r as fp16 plus m_r: exp(S_0 + S_1 - m) = E_0 * E_1 *
+// exp(m_0 + m_1 - m) * 2^-30 is exact algebra, so both CTAs form the same P
+// from identical fp16 operands (commutative products) and accumulate P . V
+// for their own half of the latent (M=128, N=256, K=64). The 2^15 shift puts
+// 28 binades below each half's maximum in fp16's normal range, and its
+// subnormals keep an absolute precision of 2^-25 below that, so each product
+// is known to a relative 2^-10 or an absolute 2^-10 (of 2^30). A row whose
+// products sum to at least 2^8 is therefore certified to within 2^-12; that
+// fails only when the two halves' scores disagree by more than about 22
+// binades. Such a row is flagged and the combine kernel recomputes it exactly
+// (16-bit caches) or it is reported as out of range (FP8 caches). No tensor-core work is
 // duplicated and no KV byte is read twice; the exchange is 16.5 KB per tile
 // and direction. (Prior art on the pages: the Hopper kernel splits O between
 // two warpgroups -- seesaw -- because the register file is full, and the FP8
@@ -92,15 +98,16 @@ constexpr uint32_t kColQ = 384;            // Q latent (bf16 pairs) at columns 3
 constexpr uint32_t kXE = 128 * 128;                     // E_r: 128 rows x 64 fp16
 constexpr uint32_t kXM = kXE;                           // + m_r per row (fp32)
 constexpr uint32_t kXMask = kXM + 128 * 4;              // + validity mask of the tile (64 bits)
-constexpr uint32_t kXFlag = kXMask + 8;                 // + 1 if this half of the tile is wide
 constexpr uint32_t kXBytes = kXMask + 16;
-// a wide half follows its message with two more: fp32 s_r - m_r of rows
-// 0-63, then of rows 64-127 (256 B per row)
-constexpr uint32_t kXPart = 64 * 256;
 // E_r = 2^(s_r - m_r + kEShift): fp16's normal range then holds every token
-// within kNarrow binades of the half's own maximum (2^-13 .. 2^15)
+// within 28 binades of the half's own maximum (2^-13 .. 2^15), and below that
+// its subnormals keep an absolute precision of 2^-25
 constexpr float kEShift = 15.0f;
-constexpr float kNarrow = 28.0f;
+// A row of a tile is certified when the sum of its products E_own E_peer is at
+// least kCertify: every product is then known to a relative 2^-10 or an
+// absolute 2^-10, so the 64 tokens' absolute errors add up to at most 2^-12 of
+// the sum (about 22 binades of disagreement between the two halves)
+constexpr float kCertify = 256.0f;
 constexpr uint32_t kXStride = 17 * 1024;
 constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
@@ -156,91 +163,6 @@ struct RowRef {
     live = Mt != -INFINITY;
   }
 };
-
-// State of one P-warp thread handed to the wide-tile path (local memory).
-struct WideIO {
-  uint32_t eo[32];  // in: this CTA's E of the row (fp16 pairs)
-  uint32_t ep[32];  // in: the peer's E of the row; out: P of the row (16-bit pairs)
-  float mt, m;      // in: m_own + m_peer, the running reference max
-  float m_use, alpha, rs;
-  int resc, js, jr;  // out: rescale flag; in/out: message counters
-};
-
-// P of one row of a wide tile, in the log domain. term k = (s_own - m_own) +
-// (s_peer - m_peer), where a narrow half gives log2(E) - kEShift and a wide
-// half the exact fp32 value of its follow-up messages. Each term is one sum
-// of two values and IEEE addition commutes, so both CTAs form the same term.
-// A thread's row lies in one follow-up part (rows 0-63, then 64-127): with
-// both halves' parts of that row resident it takes the row max, then P =
-// 2^(term + mt - m_use), reading the parts twice. Called by all four P warps
-// (they all take part in every wait and release); returns false when a wait
-// gave up. Kept out of line: it runs rarely and must not raise the register
-// demand of the common path.
-template <bool kOutF16>
-__device__ __noinline__ bool wide_tile_row(WideIO& io, bool own_wide, bool peer_wide, uint32_t xs, uint32_t xr,
-                                           int h, int pid, uint32_t bar_xsfull, uint32_t bar_xsfree,
-                                           uint32_t bar_xfull, uint32_t xempty_remote, uint32_t rank,
-                                           const Guard& guard) {
-  const int lane = h & 31;
-  const uint32_t prow = (uint32_t)(h & 63) * 256u;
-  auto side = [&](bool w, uint32_t base, const uint32_t* e, int k) -> float {
-    if (w) {
-      const float4 o = ld_shared_v4f(base + prow + ((((uint32_t)k >> 2) ^ (uint32_t)(h & 7)) << 4));
-      const int j = k & 3;
-      return j == 0 ? o.x : j == 1 ? o.y : j == 2 ? o.z : o.w;
-    }
-    const float2 f = unpack_f16x2(e[k >> 1]);
-    return log2_approx((k & 1) ? f.y : f.x) - kEShift;
-  };
-  auto term = [&](int k) { return side(own_wide, xs, io.eo, k) + side(peer_wide, xr, io.ep, k); };
-  io.rs = 0.f;
-  io.m_use = io.m;
-  io.alpha = 1.0f;
-  io.resc = 0;
-  for (int part2 = 0; part2 < 2; ++part2) {
-    const bool mine = (h >> 6) == part2;
-    if (own_wide && !warp_ok(wait(bar_xsfull, io.js & 1, guard))) return false;
-    if (peer_wide) {
-      if (pid == 0) mbar_arrive_expect_tx(bar_xfull, kXPart);
-      if (!warp_ok(wait_cluster(bar_xfull, io.jr & 1, guard))) return false;
-    }
-    uint32_t dep = 0u;
-    if (mine) {
-      float y = -INFINITY;
-#pragma unroll 1
-      for (int k = 0; k < 64; ++k) y = fmaxf(y, term(k));
-      const float Mt = (io.mt == -INFINITY || y == -INFINITY) ? -INFINITY : io.mt + y;
-      const RowRef r(io.m, Mt);
-      const float cw = r.live ? io.mt - r.m_use : 0.f;
-      float rs = 0.f;
-#pragma unroll 1
-      for (int u = 0; u < 32; ++u) {
-        const float a0 = r.live ? exp2_approx(term(2 * u) + cw) : 0.f;
-        const float a1 = r.live ? exp2_approx(term(2 * u + 1) + cw) : 0.f;
-        rs += a0 + a1;
-        io.ep[u] = kOutF16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
-        dep |= io.ep[u];
-      }
-      io.rs = rs;
-      io.m_use = r.m_use;
-      io.alpha = r.alpha;
-      io.resc = r.resc ? 1 : 0;
-    }
-    if (own_wide) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_xsfree);
-      ++io.js;
-    }
-    if (peer_wide) {
-      // the relaxed arrive must follow this warp's loads from the receive
-      // buffer: every P value depends on them
-      dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
-      if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
-      ++io.jr;
-    }
-  }
-  return true;
-}
 
 __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -676,15 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     PieceIter it(p, part);
     Piece pc;
     int g = 0, qi = 0;
-    int js = 0;  // messages this CTA has sent
     bool failed = false;
-    // XS may be (re)staged once this CTA's P warps have read message js-1 from
-    // it and the peer has read its copy (which frees the peer's receive buffer)
-    auto xs_free = [&]() {
-      return warp_ok(wait(bar(C::B_XSFREE), (js & 1) ^ 1, guard)) &&
-             warp_ok(wait_cluster(bar(C::B_XEMPTY), (js & 1) ^ 1, guard));
-    };
-    const uint32_t xs = sb + C::OFF_XS;
     while (!failed && it.next(pc)) {
       if (!load_q(pc, qi++)) break;
       MaskStream<kSparse> ms;
@@ -700,24 +614,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_SEMPTY));
-        // row max and min of the raw scores over the valid tokens (the scale
-        // is positive, so it commutes with both); masked tokens become -inf
-        // (their rows may hold NaN)
-        float lo0 = INFINITY, lo1 = INFINITY;
+        // row max of the raw scores (the scale is positive, so it commutes
+        // with the max); masked tokens become -inf (their rows may hold NaN)
         if (vm != ~0ull) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const bool v = (vm >> k) & 1ull;
-            if (k & 1) lo1 = v ? fminf(lo1, __uint_as_float(sr[k])) : lo1;
-            else lo0 = v ? fminf(lo0, __uint_as_float(sr[k])) : lo0;
-            if (!v) sr[k] = 0xFF800000u;  // -inf
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; k += 2) {
-            lo0 = fminf(lo0, __uint_as_float(sr[k]));
-            lo1 = fminf(lo1, __uint_as_float(sr[k + 1]));
-          }
+          for (int k = 0; k < 64; ++k)
+            if (!((vm >> k) & 1ull)) sr[k] = 0xFF800000u;  // -inf
         }
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -726,17 +628,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           m1 = fmaxf(m1, __uint_as_float(sr[k + 1]));
         }
         const float m_own = fmaxf(m0, m1) * sl2;
-        // wide: some valid token lies more than kNarrow binades below this
-        // half's maximum, where its fp16 factor would lose precision (false
-        // when no token is valid: +inf < -inf)
-        const bool wide = fminf(lo0, lo1) * sl2 < m_own - kNarrow;
+        // E = 2^(s - m_own + kEShift): fp16's normal range holds 28 binades
+        // below the half's maximum and its subnormals keep an absolute
+        // precision of 2^-25 below that
         const float nref = m_own == -INFINITY ? 0.f : kEShift - m_own;
         uint32_t e[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u)
           e[u] = pack_f16x2(exp2_approx(fmaf(__uint_as_float(sr[2 * u]), sl2, nref)),
                             exp2_approx(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nref)));
-        if (!xs_free()) { failed = true; break; }
+        // XS is free once this CTA's P warps have read tile g-1 from it and the
+        // peer has read its copy (which frees the peer's receive buffer too)
+        if (!warp_ok(wait(bar(C::B_XSFREE), (g & 1) ^ 1, guard)) ||
+            !warp_ok(wait_cluster(bar(C::B_XEMPTY), (g & 1) ^ 1, guard))) {
+          failed = true;
+          break;
+        }
+        const uint32_t xs = sb + C::OFF_XS;
         const uint32_t xs_row = xs + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -744,42 +652,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         reinterpret_cast<float*>(smem + C::OFF_XS + kXM)[h] = m_own;
         if (h == 0) *reinterpret_cast<uint64_t*>(smem + C::OFF_XS + kXMask) = vm;
         fence_proxy_async_smem();
-        const bool any_wide = named_sync_or(kEBar, 128, wide);
+        named_sync(kEBar, 128);
         if (h == 0) {
-          *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_XS + kXFlag) = any_wide ? 1u : 0u;
-          fence_proxy_async_smem();
           bulk_copy_to_peer(xr_remote, xs, kXBytes, xfull_remote);
           mbar_arrive(bar(C::B_XSFULL));
-        }
-        ++js;
-        if (any_wide) {
-          // Wide tile (rare: a partial-score spread of more than kNarrow
-          // binades inside one tile): the exact partial scores s_r - m_r
-          // follow as fp32, rows 0-63 and then rows 64-127, so that P can be
-          // formed in the log domain whatever the spread.
-          const float nd = m_own == -INFINITY ? 0.f : -m_own;
-          for (int part2 = 0; part2 < 2 && !failed; ++part2) {
-            if (!xs_free()) { failed = true; break; }
-            if ((h >> 6) == part2) {
-              const uint32_t row = xs + (h & 63) * 256;
-#pragma unroll
-              for (int u = 0; u < 16; ++u) {
-                float d[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) d[j] = fmaf(__uint_as_float(sr[4 * u + j]), sl2, nd);
-                st_shared_v4(row + ((u ^ (h & 7)) << 4), __float_as_uint(d[0]), __float_as_uint(d[1]),
-                             __float_as_uint(d[2]), __float_as_uint(d[3]));
-              }
-            }
-            fence_proxy_async_smem();
-            named_sync(kEBar, 128);
-            if (h == 0) {
-              bulk_copy_to_peer(xr_remote, xs, kXPart, xfull_remote);
-              mbar_arrive(bar(C::B_XSFULL));
-            }
-            ++js;
-          }
-          if (failed) break;
         }
       }
     }
@@ -794,16 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     PieceIter it(p, part);
     Piece pc;
     int g = 0, pcount = 0;
-    int js = 0, jr = 0;  // own messages read from XS, peer messages read from XR
     bool failed = false;
-    // Hand the receive buffer back to the peer. The arrive is relaxed, so it
-    // must not be performed before this warp's loads from the buffer have
-    // returned: its address depends on every loaded value (through a mask that
-    // is zero at run time, the rank being 0 or 1).
-    auto release_xr = [&](uint32_t dep) {
-      dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
-      if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
-    };
     while (!failed && it.next(pc)) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       float m = -INFINITY, l = 0.f;
@@ -811,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         // (1) this CTA's own E and m of tile g, staged by the E warps (always
         // before the peer's copy of the same tile lands, so read first)
         uint32_t ep[32], eo[32];
-        if (!warp_ok(wait(bar(C::B_XSFULL), js & 1, guard))) { failed = true; break; }
+        if (!warp_ok(wait(bar(C::B_XSFULL), g & 1, guard))) { failed = true; break; }
         const uint32_t xs_row = sb + C::OFF_XS + h * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -821,12 +688,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
         const float m_own = reinterpret_cast<const float*>(smem + C::OFF_XS + kXM)[h];
         const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + kXMask);
-        const bool own_wide = *reinterpret_cast<const volatile uint32_t*>(smem + C::OFF_XS + kXFlag) != 0u;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_XSFREE));
-        ++js;
-        // a[k]: the product E_own E_peer of token k (linear, up to 2^(2 kEShift)),
-        // or for a wide tile (s_own - m_own) + (s_peer - m_peer) (log2 domain).
+        // a[k]: the product E_own E_peer of token k, up to 2^(2 kEShift).
         // 16-bit caches unpack their own E while the peer's message is on its
         // way; FP8 caches (128 registers a thread) unpack it as it is used.
         float a[64];
@@ -844,7 +708,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         };
         // (2) the peer's E and m of tile g
         if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
-        if (!warp_ok(wait_cluster(bar(C::B_XFULL), jr & 1, guard))) { failed = true; break; }
+        if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 o = ld_shared_v4f(xr_row + ((u ^ (h & 7)) << 4));
@@ -852,79 +716,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           ep[4 * u + 2] = __float_as_uint(o.z); ep[4 * u + 3] = __float_as_uint(o.w);
         }
         const float m_peer = xr_m[h];
-        const uint32_t peer_flag = *reinterpret_cast<const volatile uint32_t*>(smem + C::OFF_XR + kXFlag);
         {
-          uint32_t dep = __float_as_uint(m_peer) | peer_flag;
+          // Hand the receive buffer back to the peer. The arrive is relaxed,
+          // so it must not be performed before this warp's loads from the
+          // buffer have returned: its address depends on every loaded value
+          // (through a mask that is zero at run time, the rank being 0 or 1).
+          uint32_t dep = __float_as_uint(m_peer);
 #pragma unroll
           for (int u = 0; u < 8; ++u) dep |= ep[4 * u];
-          release_xr(dep);
+          dep = __reduce_or_sync(0xffffffffu, dep) & (rank >> 1);
+          if (lane == 0) mbar_arrive_remote_relaxed(xempty_remote + dep);
         }
-        ++jr;
-        const bool peer_wide = peer_flag != 0u;
-        // (3) the tile's row max Mt relative to mt = m_own + m_peer (an upper
-        // bound of it, far above it when the halves peak on different
-        // tokens), then P = 2^(s - m_use) against the running reference max
+        // (3) P = 2^(s - m_use) against the running reference max m_use,
+        // moved lazily (P <= 256). mt = m_own + m_peer bounds the tile's row
+        // max from above, far above it when the halves peak on different
+        // tokens. S = sum of the products certifies the row (kCertify).
         const float mt = m_own + m_peer;
-        float m_use, alpha, rs0 = 0.f, rs1 = 0.f;
-        bool resc;
-        if (!(own_wide || peer_wide)) {  // the same in every thread of both CTAs
-          // both halves narrow: every valid factor is a normal fp16 value
-          // (relative error 2^-11) and the product is exact in fp32
-          float p0 = 0.f, p1 = 0.f;
+        float m_use, alpha, rs0;
+        bool resc, cert;
+        if constexpr (!(kFp16 || kFp8)) {
+          // bf16 P keeps fp32's exponent range: the reference may sit far
+          // above the tile's row max, so take mt and go in one pass
+          const RowRef r(m, mt);
+          m_use = r.m_use;
+          alpha = r.alpha;
+          resc = r.resc;
+          const float cf = r.live ? exp2_approx((mt - m_use) - 2.f * kEShift) : 0.f;
+          float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float2 fq = unpack_f16x2(ep[u]);
+            const float2 fw = own_pair(u);
+            const float a0 = fw.x * fq.x * cf, a1 = fw.y * fq.y * cf;
+            rs[(2 * u) & 7] += a0;
+            rs[(2 * u + 1) & 7] += a1;
+            ep[u] = pack_bf16x2(a0, a1);
+          }
+          rs0 = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+          // (cf = 0: no valid token, or a tile more than 2^126 below the row)
+          cert = !(cf > 0.f) || rs0 >= kCertify * cf;
+        } else {
+          // fp16 P ends at 2^-24: the reference comes from S, which puts the
+          // tile's row max within 6 binades: mt - 2 kEShift + log2 S - 6 <= Mt
+          float sv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const float2 fq = unpack_f16x2(ep[u]);
             const float2 fw = own_pair(u);
             a[2 * u] = fw.x * fq.x;
             a[2 * u + 1] = fw.y * fq.y;
-            p0 = fmaxf(p0, a[2 * u]);
-            p1 = fmaxf(p1, a[2 * u + 1]);
+            sv[(2 * u) & 7] += a[2 * u];
+            sv[(2 * u + 1) & 7] += a[2 * u + 1];
           }
-          const float pm = fmaxf(p0, p1);
-          const float Y = pm > 0.f ? log2_approx(pm) - 2.f * kEShift : -INFINITY;
-          const RowRef r(m, (mt == -INFINITY || Y == -INFINITY) ? -INFINITY : mt + Y);
+          const float S = ((sv[0] + sv[1]) + (sv[2] + sv[3])) + ((sv[4] + sv[5]) + (sv[6] + sv[7]));
+          const RowRef r(m, (mt == -INFINITY || !(S > 0.f)) ? -INFINITY : mt + (log2_approx(S) - 2.f * kEShift));
           m_use = r.m_use;
           alpha = r.alpha;
           resc = r.resc;
-          // P = a * 2^(mt - 2 kEShift - m_use)
           const float cf = r.live ? exp2_approx((mt - m_use) - 2.f * kEShift) : 0.f;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float a0 = a[2 * u] * cf, a1 = a[2 * u + 1] * cf;
-            rs0 += a0;
-            rs1 += a1;
-            ep[u] = (kFp16 || kFp8) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
-          }
-        } else {
-          // a wide tile (a half whose valid scores spread over more than
-          // kNarrow binades): exact log-domain P, out of line
-          WideIO io;
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            if constexpr (kFp8) io.eo[u] = eo[u];
-            else io.eo[u] = pack_f16x2(a[2 * u], a[2 * u + 1]);  // exact round trip
-            io.ep[u] = ep[u];
-          }
-          io.mt = mt;
-          io.m = m;
-          io.js = js;
-          io.jr = jr;
-          if (!wide_tile_row<kFp16 || kFp8>(io, own_wide, peer_wide, sb + C::OFF_XS, sb + C::OFF_XR, h, pid,
-                                             bar(C::B_XSFULL), bar(C::B_XSFREE), bar(C::B_XFULL), xempty_remote,
-                                             rank, guard)) {
-            failed = true;
-            break;
-          }
-          js = io.js;
-          jr = io.jr;
-#pragma unroll
-          for (int u = 0; u < 32; ++u) ep[u] = io.ep[u];
-          m_use = io.m_use;
-          alpha = io.alpha;
-          resc = io.resc != 0;
-          rs0 = io.rs;
+          for (int u = 0; u < 32; ++u) ep[u] = pack_f16x2(a[2 * u] * cf, a[2 * u + 1] * cf);
+          rs0 = S * cf;
+          cert = !r.live || S >= kCertify;
         }
-        l = l * alpha + (rs0 + rs1);
+        {
+          // The halves disagree by more than about 22 binades on a row
+          // (rare): the row's result from here on is not certified. For
+          // 16-bit caches the row is flagged, and the combine kernel
+          // recomputes it exactly from q and the cache rows; FP8 caches report
+          // it. (Kept out of this kernel: its slow path would cost the common
+          // one registers and code.)
+          const uint32_t unc = __ballot_sync(0xffffffffu, !cert);
+          if (unc != 0u && rank == 0 && lane == 0) {
+            if constexpr (kFp8 || kSparse) atomicOr(p.status, STATUS_RANGE);
+            else atomicOr(p.exact_flags + (int64_t)pc.v * 4 + (warp - 8), unc);
+          }
+        }
+        l = l * alpha + rs0;
         m = m_use;
         // a rescale of O needs every earlier P . V done; they complete in issue
         // order, so waiting for tile g-1 is enough

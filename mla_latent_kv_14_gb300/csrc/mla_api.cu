@@ -193,8 +193,7 @@ size_t mla_metadata_size(int batch, int s_q, int parts) {
 
 size_t mla_workspace_size(int batch, int s_q, int h_q, int parts) {
   if (batch <= 0 || s_q <= 0 || h_q <= 0 || parts <= 0) return 0;
-  const int64_t S = max_splits(batch * s_q, parts);
-  return kWsHeader + (size_t)S * h_q * kDV * sizeof(float) + (size_t)S * h_q * sizeof(float);
+  return ws_bytes(batch * s_q, parts, h_q);
 }
 
 mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int h_kv, int topk,
@@ -337,7 +336,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.block_table = block_table;
   p.seqlens = cache_seqlens;
   p.indices = indices;
-  p.kv_fp8 = static_cast<const uint8_t*>(kvcache);
+  p.kv = static_cast<const uint8_t*>(kvcache);
   p.meta = static_cast<const int32_t*>(metadata);
   p.split_off = num_splits;
   p.out = out;
@@ -346,6 +345,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.o_part = reinterpret_cast<float*>(ws + kWsHeader);
   p.lse_part = p.o_part + S * h_q * kDV;
+  p.exact_flags = reinterpret_cast<uint32_t*>(ws + ws_flags_offset(batch * s_q, parts, h_q));
   p.num_blocks = num_blocks;
   p.num_rows = num_blocks * page_block;
   p.max_blocks = max_blocks;
@@ -408,6 +408,17 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
 
   // combine, overlapped with the decode grid's tail (programmatic dependent launch)
   CombineParams c{num_splits, p.o_part, p.lse_part, out, lse, batch, s_q, h_q, fp16 ? 1 : 0};
+  if (!is_fp8 && !indices && h_q == 128) {  // the kernels that flag rows for an exact recompute
+    c.exact_flags = p.exact_flags;
+    c.q = q;
+    c.kv = p.kv;
+    c.block_table = block_table;
+    c.seqlens = cache_seqlens;
+    c.num_blocks = num_blocks;
+    c.max_blocks = max_blocks;
+    c.causal = causal ? 1 : 0;
+    c.scale_log2 = p.scale_log2;
+  }
   cudaLaunchConfig_t cc = {};
   cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, 1);
   cc.blockDim = dim3(256, 1, 1);

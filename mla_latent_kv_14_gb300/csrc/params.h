@@ -36,9 +36,19 @@ __host__ __device__ inline uint32_t hash_step(uint32_t h, uint32_t x) {
 
 // ---- workspace ----
 // [0, 256): status word; then o_part fp32 [max_splits, h_q, 512]; then
-// lse_part fp32 [max_splits, h_q]
+// lse_part fp32 [max_splits, h_q]; then the exact-recompute flags uint32
+// [vreq][4]: one bit per head (h_q <= 128), set by the decode kernel for a row
+// it could not certify and cleared by the combine kernel once it has
+// recomputed that row exactly (zero between calls)
 constexpr size_t kWsHeader = 256;
 __host__ __device__ inline int64_t max_splits(int vreq, int parts) { return (int64_t)vreq + parts; }
+__host__ __device__ inline size_t ws_flags_offset(int vreq, int parts, int h_q) {
+  const int64_t S = max_splits(vreq, parts);
+  return kWsHeader + (size_t)S * h_q * 512 * sizeof(float) + (size_t)S * h_q * sizeof(float);
+}
+__host__ __device__ inline size_t ws_bytes(int vreq, int parts, int h_q) {
+  return ws_flags_offset(vreq, parts, h_q) + (size_t)vreq * 4 * sizeof(uint32_t);
+}
 
 struct MetaParams {
   const int32_t* seqlens;   // [batch] or null (sparse)
@@ -52,7 +62,7 @@ struct DecodeParams {
   const int32_t* block_table;  // [batch, max_blocks] (dense)
   const int32_t* seqlens;      // [batch]
   const int32_t* indices;      // [batch, s_q, topk] (sparse) or null
-  const uint8_t* kv_fp8;       // raw fp8 rows (fp8 kernels)
+  const uint8_t* kv;           // the cache rows as bytes (1152-B 16-bit or 656-B FP8 rows)
   const int32_t* meta;
   const int32_t* split_off;
   void* out;                   // [batch, s_q, h_q, 512], q dtype
@@ -60,6 +70,7 @@ struct DecodeParams {
   float* o_part;               // [max_splits, h_q, 512]
   float* lse_part;             // [max_splits, h_q]
   uint32_t* status;
+  uint32_t* exact_flags;       // [vreq][4] head bits of rows to recompute exactly
   int64_t num_blocks;
   int64_t num_rows;            // num_blocks * page_block
   int max_blocks;
@@ -80,6 +91,17 @@ struct CombineParams {
   float* lse;
   int batch, s_q, h_q;
   int fp16;
+  // exact recompute of the rows the decode kernel flagged (dense 16-bit
+  // caches; null otherwise): q, the cache rows (1152 B each), block table and
+  // lengths of the call
+  uint32_t* exact_flags;
+  const void* q;
+  const uint8_t* kv;
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  int64_t num_blocks;
+  int max_blocks, causal;
+  float scale_log2;
 };
 
 }  // namespace mla

@@ -294,6 +294,17 @@ MLA_DEV void tmem_st32x4(uint32_t taddr, const uint32_t* r) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) tmem_st32(taddr + 32u * c, r + 32 * c);
 }
+// 32 lanes x 8 consecutive columns
+MLA_DEV void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+MLA_DEV void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 MLA_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // keep uses of registers filled by an asynchronous tcgen05.ld after the wait
 MLA_DEV void pin_regs32(uint32_t* r) {
@@ -382,6 +393,46 @@ MLA_DEV float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// three-input max / min (IEEE maxNum / minNum: a NaN operand is ignored)
+MLA_DEV float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+MLA_DEV float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max / min of 64 values as balanced trees of three-input ops (depth 4, 32
+// ops each): a reduction on a warp's critical path costs its depth in
+// latency, and a serial chain of 32 would cost eight times more
+template <class F>
+MLA_DEV float tree_max64(F v) {
+  float t[22];
+#pragma unroll
+  for (int j = 0; j < 21; ++j) t[j] = max3(v(3 * j), v(3 * j + 1), v(3 * j + 2));
+  t[21] = v(63);
+  float u[8];
+#pragma unroll
+  for (int j = 0; j < 7; ++j) u[j] = max3(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+  u[7] = t[21];
+  return max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+}
+template <class F>
+MLA_DEV float tree_min64(F v) {
+  float t[22];
+#pragma unroll
+  for (int j = 0; j < 21; ++j) t[j] = min3(v(3 * j), v(3 * j + 1), v(3 * j + 2));
+  t[21] = v(63);
+  float u[8];
+#pragma unroll
+  for (int j = 0; j < 7; ++j) u[j] = min3(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+  u[7] = t[21];
+  return min3(min3(u[0], u[1], u[2]), min3(u[3], u[4], u[5]), fminf(u[6], u[7]));
 }
 
 MLA_DEV float log2_approx(float x) {

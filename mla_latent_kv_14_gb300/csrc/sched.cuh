@@ -362,6 +362,113 @@ struct MaskStream {
   }
 };
 
+// ---- exact recompute of flagged rows (dense 16-bit caches) ----
+// The decode kernel flags a (query position, head) row when the two halves of
+// its scores disagree too much for the fp16 factors the pair exchanges; the
+// combine recomputes such a row here, from q and the cache rows, with plain
+// fp32 arithmetic.
+template <bool kF16>
+__device__ __forceinline__ float half_to_f32(uint32_t bits16) {
+  if constexpr (kF16) return __half2float(__ushort_as_half((unsigned short)bits16));
+  else return __uint_as_float(bits16 << 16);
+}
+// q . K over the 576 dims of 16-bit rows, in fp32 and a fixed order
+template <bool kF16>
+__device__ __forceinline__ float dot576(const uint16_t* q, const uint16_t* k) {
+  const uint4* qa = reinterpret_cast<const uint4*>(q);
+  const uint4* ka = reinterpret_cast<const uint4*>(k);
+  float acc = 0.f;
+#pragma unroll 2
+  for (int c = 0; c < kDK / 8; ++c) {
+    const uint4 x = __ldg(qa + c), y = __ldg(ka + c);
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc = fmaf(half_to_f32<kF16>(xw[j] & 0xFFFFu), half_to_f32<kF16>(yw[j] & 0xFFFFu), acc);
+      acc = fmaf(half_to_f32<kF16>(xw[j] >> 16), half_to_f32<kF16>(yw[j] >> 16), acc);
+    }
+  }
+  return acc;
+}
+
+// Attention of head h of query position i of request b over all its visible
+// tokens, by the whole block (256 threads): an online softmax over chunks of
+// 256 tokens, one exact score per thread, then each thread accumulates two of
+// the 512 output dims over the chunk. Pages out of range are skipped, as in
+// the decode kernel.
+template <typename OutT>
+__device__ void exact_head(const CombineParams& p, int b, int i, int h) {
+  constexpr bool kF16 = std::is_same<OutT, __half>::value;
+  __shared__ float sP[256];
+  __shared__ int64_t sRow[256];
+  __shared__ float red_m[8], red_s[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int L = p.seqlens[b];
+  if (p.causal) L = L - p.s_q + 1 + i;
+  L = L < 0 ? 0 : L;
+  const int64_t qv = (int64_t)b * p.s_q + i;
+  const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + (qv * p.h_q + h) * kDK;
+  const uint16_t* kv = reinterpret_cast<const uint16_t*>(p.kv);
+  float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f;
+  for (int c0 = 0; c0 < L; c0 += 256) {
+    const int t = c0 + tid;
+    float s = -INFINITY;
+    int64_t row = -1;
+    if (t < L && t / kTile < p.max_blocks) {
+      const int page = __ldg(p.block_table + (int64_t)b * p.max_blocks + t / kTile);
+      if (page >= 0 && page < p.num_blocks) {
+        row = (int64_t)page * kTile + t % kTile;
+        s = dot576<kF16>(qrow, kv + row * kDK) * p.scale_log2;
+      }
+    }
+    float mx = s;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_m[warp] = mx;
+    __syncthreads();
+    mx = red_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red_m[w]);
+    const float m_new = fmaxf(m, mx);
+    const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+    const float pt = (s == -INFINITY) ? 0.f : exp2f(s - m_new);
+    sP[tid] = pt;
+    sRow[tid] = row;
+    float sm = pt;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) red_s[warp] = sm;
+    __syncthreads();
+    sm = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sm += red_s[w];
+    l = l * alpha + sm;
+    o0 *= alpha;
+    o1 *= alpha;
+    const int n = L - c0 < 256 ? L - c0 : 256;
+    for (int j = 0; j < n; ++j) {
+      const float pj = sP[j];
+      if (pj != 0.f) {
+        const uint16_t* vr = kv + sRow[j] * kDK;
+        o0 = fmaf(pj, half_to_f32<kF16>(vr[tid]), o0);
+        o1 = fmaf(pj, half_to_f32<kF16>(vr[tid + 256]), o1);
+      }
+    }
+    m = m_new;
+    __syncthreads();
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  OutT* orow = reinterpret_cast<OutT*>(p.out) + (qv * p.h_q + h) * kDV;
+  if constexpr (kF16) {
+    orow[tid] = __float2half_rn(o0 * inv);
+    orow[tid + 256] = __float2half_rn(o1 * inv);
+  } else {
+    orow[tid] = __float2bfloat16_rn(o0 * inv);
+    orow[tid + 256] = __float2bfloat16_rn(o1 * inv);
+  }
+  if (tid == 0) p.lse[qv * p.h_q + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+}
+
 // Merge the split partials of each virtual request. grid = (vreq, h_q/16),
 // block = 256: each warp merges two heads, each lane 16 of the 512 dims.
 // Requests with a single piece were finished by the decode kernel; requests
@@ -374,6 +481,19 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   pdl_wait();  // the decode grid has completed and its writes are visible
   const int v = blockIdx.x;
   const int b = v % p.batch, i = v / p.batch;
+  // rows the decode kernel flagged (bit k: head 16*blockIdx.y + k) are
+  // recomputed exactly and left out of the merge below; their bits are cleared
+  uint32_t fmask = 0u;
+  if (p.exact_flags) {
+    const int h0 = blockIdx.y * 16;
+    uint32_t* fw = p.exact_flags + (int64_t)v * 4 + (h0 >> 5);
+    fmask = (*fw >> (h0 & 31)) & 0xFFFFu;
+    if (fmask) {
+      for (int k = 0; k < 16; ++k)
+        if ((fmask >> k) & 1u) exact_head<OutT>(p, b, i, h0 + k);
+      if (threadIdx.x == 0) atomicAnd(fw, ~(0xFFFFu << (h0 & 31)));
+    }
+  }
   const int off = p.split_off[v];
   const int ns = p.split_off[v + 1] - off;
   if (ns == 1) return;
@@ -381,6 +501,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   for (int hh = 0; hh < 2; ++hh) {
     const int h = blockIdx.y * 16 + warp * 2 + hh;
     if (h >= p.h_q) break;
+    if ((fmask >> (warp * 2 + hh)) & 1u) continue;  // recomputed above
     const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
     OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
     auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };

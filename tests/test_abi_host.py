@@ -55,7 +55,7 @@ def test_status_strings(lib):
 def test_sizes(lib):
     assert lib.mla_metadata_size(64, 1, 76) == 4 * (16 + 8 * 76)
     ws = lib.mla_workspace_size(64, 1, 128, 76)
-    assert ws == 256 + (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4
+    assert ws == 256 + (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4 + 64 * 16
     assert lib.mla_workspace_size(0, 1, 128, 76) == 0
 
 

@@ -11,7 +11,9 @@ request whose partial scores disagree by delta log2 units: token A holds the
 first half's maximum and its second-half score lies delta below the second
 half's maximum, token B the other way round, and A and B win the full score
 by 8 log2 units. The signal lives in the RoPE dims, which are not part of
-the value, so the output stays an average of N(0,1) rows.
+the value, so the output stays an average of N(0,1) rows. Delta 12 and 20
+stay within what the fp16 factors certify; delta 30 and 60 go beyond it, where
+16-bit caches recompute the row exactly and FP8 caches report it.
 """
 import numpy as np
 import pytest
@@ -137,17 +139,23 @@ def test_every_token_split(parts):
 @pytest.mark.parametrize("delta", [20, 60])
 def test_split_peaks_fp16(delta):
     """fp16 caches carry P as fp16, whose range ends at 2^-24: the reference
-    max must be the tile's true max, not the sum of the halves' maxima."""
+    max must lie near the tile's true max, not at the sum of the halves'
+    maxima."""
     case, _ = dense_case(delta, dtype=torch.float16, seed=62)
     out, lse = run_dense(case)
     ro, rl = oracle_dense(case)
     assert_close_attn(out, lse, ro, rl, f"fp16 split peaks delta={delta}")
 
 
-@pytest.mark.parametrize("delta", [20, 60])
+MLA_ERR_RANGE = 7
+
+
+@pytest.mark.parametrize("delta", [12, 60])
 def test_split_peaks_fp8_dense(delta):
     """The RoPE dims of the 656-byte row stay bf16, so the planted signal
-    survives quantisation; compared with the oracle on the dequantised cache."""
+    survives quantisation. FP8 caches certify a row when its halves disagree
+    by up to about 22 binades (delta 12: compared with the oracle on the
+    dequantised cache) and report the rows beyond that (delta 60)."""
     case, _ = dense_case(delta, seed=63)
     raw = mla.mla_quantize_kv_fp8(case.kv_rows.to(DEV))
     deq = oracle.dequantize_kv_fp8(oracle.quantize_kv_fp8(case.kv_rows))
@@ -158,13 +166,17 @@ def test_split_peaks_fp8_dense(delta):
                                            case.block_table.to(DEV), sl, 512, meta, ns,
                                            softmax_scale=case.softmax_scale, is_fp8=True)
     torch.cuda.synchronize()
-    assert mla.mla_read_status(device=DEV)[0] == 0
+    st, bits = mla.mla_read_status(device=DEV)
+    if delta > 22:
+        assert st == MLA_ERR_RANGE and bits & 8, (st, bits)
+        return
+    assert st == 0, (st, bits)
     ro, rl, _ = oracle.mla_decode(oracle.to_f64(case.q), deq, cache_seqlens=case.cache_seqlens.numpy(),
                                   block_table=case.block_table.numpy(), softmax_scale=case.softmax_scale)
     assert_close_attn(out, lse, ro, rl, f"fp8 dense split peaks delta={delta}")
 
 
-@pytest.mark.parametrize("delta", [20, 60])
+@pytest.mark.parametrize("delta", [12, 60])
 def test_split_peaks_fp8_sparse(delta):
     case = synth.make_sparse_case(2, 2, 192, tokens_per_request=1024, seed=64)
     idx = case.indices.numpy()
@@ -178,6 +190,10 @@ def test_split_peaks_fp8_sparse(delta):
                                            softmax_scale=case.softmax_scale, is_fp8=True,
                                            indices=case.indices.to(DEV))
     torch.cuda.synchronize()
-    assert mla.mla_read_status(device=DEV)[0] == 0
+    st, bits = mla.mla_read_status(device=DEV)
+    if delta > 22:
+        assert st == MLA_ERR_RANGE and bits & 8, (st, bits)
+        return
+    assert st == 0, (st, bits)
     ro, rl, _ = oracle.mla_decode(oracle.to_f64(case.q), deq, indices=idx, softmax_scale=case.softmax_scale)
     assert_close_attn(out, lse, ro, rl, f"fp8 sparse split peaks delta={delta}")
