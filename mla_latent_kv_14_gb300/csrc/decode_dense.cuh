@@ -621,22 +621,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           for (int k = 0; k < 64; ++k)
             if (!((vm >> k) & 1ull)) sr[k] = 0xFF800000u;  // -inf
         }
-        float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          m0 = fmaxf(m0, __uint_as_float(sr[k]));
-          m1 = fmaxf(m1, __uint_as_float(sr[k + 1]));
-        }
-        const float m_own = fmaxf(m0, m1) * sl2;
+        const float m_own = tree_max64([&](int k) { return __uint_as_float(sr[k]); }) * sl2;
         // E = 2^(s - m_own + kEShift): fp16's normal range holds 28 binades
         // below the half's maximum and its subnormals keep an absolute
         // precision of 2^-25 below that
         const float nref = m_own == -INFINITY ? 0.f : kEShift - m_own;
+        // the exponents two tokens per instruction (packed fp32 pairs)
+        const uint64_t sl2_2 = f2_pack(sl2, sl2), nref2 = f2_pack(nref, nref);
         uint32_t e[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          e[u] = pack_f16x2(exp2_approx(fmaf(__uint_as_float(sr[2 * u]), sl2, nref)),
-                            exp2_approx(fmaf(__uint_as_float(sr[2 * u + 1]), sl2, nref)));
+        for (int u = 0; u < 32; ++u) {
+          const float2 x = f2_unpack(
+              f2_fma(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), sl2_2, nref2));
+          e[u] = pack_f16x2(exp2_approx(x.x), exp2_approx(x.y));
+        }
         // XS is free once this CTA's P warps have read tile g-1 from it and the
         // peer has read its copy (which frees the peer's receive buffer too)
         if (!warp_ok(wait(bar(C::B_XSFREE), (g & 1) ^ 1, guard)) ||
@@ -690,22 +688,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         const uint64_t vm = *reinterpret_cast<const volatile uint64_t*>(smem + C::OFF_XS + kXMask);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_XSFREE));
-        // a[k]: the product E_own E_peer of token k, up to 2^(2 kEShift).
-        // 16-bit caches unpack their own E while the peer's message is on its
-        // way; FP8 caches (128 registers a thread) unpack it as it is used.
-        float a[64];
-        if constexpr (!kFp8) {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float2 f = unpack_f16x2(eo[u]);
-            a[2 * u] = f.x;
-            a[2 * u + 1] = f.y;
-          }
-        }
-        auto own_pair = [&](int u) {
-          if constexpr (kFp8) return unpack_f16x2(eo[u]);
-          else return make_float2(a[2 * u], a[2 * u + 1]);
-        };
         // (2) the peer's E and m of tile g
         if (pid == 0) mbar_arrive_expect_tx(bar(C::B_XFULL), kXBytes);
         if (!warp_ok(wait_cluster(bar(C::B_XFULL), g & 1, guard))) { failed = true; break; }
@@ -732,6 +714,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         // max from above, far above it when the halves peak on different
         // tokens. S = sum of the products certifies the row (kCertify).
         const float mt = m_own + m_peer;
+        // the products E_own E_peer of a token pair, up to 2^(2 kEShift), in
+        // one mixed-precision fma each (exact, and the same in both CTAs)
+        auto prod = [&](int u) { return mul_f16x2_to_f32(eo[u], ep[u]); };
         float m_use, alpha, rs0;
         bool resc, cert;
         if constexpr (!(kFp16 || kFp8)) {
@@ -742,40 +727,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           alpha = r.alpha;
           resc = r.resc;
           const float cf = r.live ? exp2_approx((mt - m_use) - 2.f * kEShift) : 0.f;
-          float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          // P and the row sum two tokens per instruction (packed fp32 pairs;
+          // four partial sums keep the dependency chains short)
+          const uint64_t cf2 = f2_pack(cf, cf);
+          uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float2 fq = unpack_f16x2(ep[u]);
-            const float2 fw = own_pair(u);
-            const float a0 = fw.x * fq.x * cf, a1 = fw.y * fq.y * cf;
-            rs[(2 * u) & 7] += a0;
-            rs[(2 * u + 1) & 7] += a1;
-            ep[u] = pack_bf16x2(a0, a1);
+            const float2 e = prod(u);
+            const uint64_t p2 = f2_mul(f2_pack(e.x, e.y), cf2);
+            rs2[u & 3] = f2_add(rs2[u & 3], p2);
+            const float2 pp = f2_unpack(p2);
+            ep[u] = pack_bf16x2(pp.x, pp.y);
           }
-          rs0 = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+          const float2 r01 = f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])));
+          rs0 = r01.x + r01.y;
           // (cf = 0: no valid token, or a tile more than 2^126 below the row)
           cert = !(cf > 0.f) || rs0 >= kCertify * cf;
         } else {
           // fp16 P ends at 2^-24: the reference comes from S, which puts the
           // tile's row max within 6 binades: mt - 2 kEShift + log2 S - 6 <= Mt
-          float sv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          uint64_t a2[32];
+          uint64_t sv2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float2 fq = unpack_f16x2(ep[u]);
-            const float2 fw = own_pair(u);
-            a[2 * u] = fw.x * fq.x;
-            a[2 * u + 1] = fw.y * fq.y;
-            sv[(2 * u) & 7] += a[2 * u];
-            sv[(2 * u + 1) & 7] += a[2 * u + 1];
+            const float2 e = prod(u);
+            a2[u] = f2_pack(e.x, e.y);
+            sv2[u & 3] = f2_add(sv2[u & 3], a2[u]);
           }
-          const float S = ((sv[0] + sv[1]) + (sv[2] + sv[3])) + ((sv[4] + sv[5]) + (sv[6] + sv[7]));
+          const float2 s01 = f2_unpack(f2_add(f2_add(sv2[0], sv2[1]), f2_add(sv2[2], sv2[3])));
+          const float S = s01.x + s01.y;
           const RowRef r(m, (mt == -INFINITY || !(S > 0.f)) ? -INFINITY : mt + (log2_approx(S) - 2.f * kEShift));
           m_use = r.m_use;
           alpha = r.alpha;
           resc = r.resc;
           const float cf = r.live ? exp2_approx((mt - m_use) - 2.f * kEShift) : 0.f;
+          const uint64_t cf2 = f2_pack(cf, cf);
 #pragma unroll
-          for (int u = 0; u < 32; ++u) ep[u] = pack_f16x2(a[2 * u] * cf, a[2 * u + 1] * cf);
+          for (int u = 0; u < 32; ++u) {
+            const float2 pp = f2_unpack(f2_mul(a2[u], cf2));
+            ep[u] = pack_f16x2(pp.x, pp.y);
+          }
           rs0 = S * cf;
           cert = !r.live || S >= kCertify;
         }
@@ -842,14 +833,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       // each thread writes 32 consecutive values of its own row per chunk;
       // 32-byte stores make every request of a warp a whole sector, and the
       // TMEM load of chunk cc+1 is in flight while chunk cc is stored
+      const uint64_t inv2 = f2_pack(inv_l, inv_l);
       auto store_chunk = [&](int cc, uint32_t* r) {
         if (pc.fin) {
           OutT* dst = reinterpret_cast<OutT*>(p.out) + row * kDV + 256 * rank + 32 * cc;
           uint32_t w[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float a = __uint_as_float(r[2 * k]) * inv_l, c = __uint_as_float(r[2 * k + 1]) * inv_l;
-            w[k] = kFp16 ? pack_f16x2(a, c) : pack_bf16x2(a, c);
+            const float2 ac = f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), inv2));
+            w[k] = kFp16 ? pack_f16x2(ac.x, ac.y) : pack_bf16x2(ac.x, ac.y);
           }
           if (p.out_v8) {
             st_global_v8(dst, w);
@@ -862,7 +854,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         } else {
           float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * cc;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * inv_l);
+          for (int k = 0; k < 32; k += 2) {
+            const float2 ac = f2_unpack(f2_mul(f2_pack(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), inv2));
+            r[k] = __float_as_uint(ac.x);
+            r[k + 1] = __float_as_uint(ac.y);
+          }
 #pragma unroll
           for (int k = 0; k < 32; k += 8) st_global_v8(dst + k, r + k);
         }

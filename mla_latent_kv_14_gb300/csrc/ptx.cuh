@@ -457,6 +457,44 @@ MLA_DEV float2 unpack_f16x2(uint32_t v) {
       : "=f"(r.x), "=f"(r.y) : "r"(v));
   return r;
 }
+// packed fp32 pairs (one 64-bit register, low word first): the f32x2
+// arithmetic does two lanes' worth of work per instruction
+MLA_DEV uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+MLA_DEV float2 f2_unpack(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+MLA_DEV uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+MLA_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+MLA_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// the two products x.lo * y.lo and x.hi * y.hi of fp16 pairs, in fp32 (exact:
+// mixed-precision fma with fp16 inputs and a zero fp32 addend)
+MLA_DEV float2 mul_f16x2_to_f32(uint32_t x, uint32_t y) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {yl, yh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, xl, yl, 0f00000000;\n\tfma.rn.f32.f16 %1, xh, yh, 0f00000000;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(x), "r"(y));
+  return make_float2(lo, hi);
+}
+
 MLA_DEV uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
