@@ -21,6 +21,11 @@ What it computes, and where the pages say so
 * FP8 row: 512 e4m3 values quantised per 128 with one fp32 scale each, then 4
   fp32 scales, then the 64 RoPE dims kept as bf16; 656 bytes ("FlashMLA 实战",
   §FP8 缓存怎么把 KV 压掉四成; 拆解 page §八 '格式').
+* V4.1 rows (拆解 page §八 '版本漂移', §十 format table): 528 bytes = 512 e4m3
+  values then 16 UE8M0 scales (2^(byte-127), one per 32 values, RoPE part
+  quantised too); the FP4 option, 288 bytes = 512 e2m1 values two to a byte
+  then 32 e4m3 scales (one per 16 values). These rows hold 512 values in all,
+  so a V4.1 key is 512 wide and its value is the whole row (d_k = d_v = 512).
 
 Readings where the pages are silent:
 * causal with s_q > 1 is bottom-right aligned: query i of s_q sees tokens
@@ -31,6 +36,13 @@ Readings where the pages are silent:
   block is all zero), code = e4m3 round-to-nearest-even of x / scale,
   saturated to +-448;
 * an out-of-range index or page entry is skipped (and reported).
+* the 528-byte quantiser: the scale is the smallest power of two 2^k
+  (k >= -127) with 448 * 2^k >= amax (the pages' UE8M0 rule: a power-of-two
+  scale rounded up, 拆解 page §三), code = e4m3 round-to-nearest-even of x/2^k;
+* the 288-byte quantiser: the scale is the smallest non-negative e4m3 value v
+  with 6 v >= amax (rounded up, like the UE8M0 scale), 448 when none is large
+  enough (values then saturate to +-6); code = e2m1 round-to-nearest-even of
+  x/v with the sign of x; value 2i in the low nibble of byte i.
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 something other than itself (closed forms, the pages' other formulations,
@@ -163,6 +175,137 @@ def dequantize_kv_fp8(raw: np.ndarray) -> np.ndarray:
     out[:, :_LAT] = (vals * scale[:, :, None]).reshape(n, _LAT)
     out[:, _LAT:] = bf16_to_f64(raw[:, _LAT + 16:].copy().view("<u2"))
     return out
+
+
+# ----------------------------------------------------------------------------
+# V4.1 cache rows of 512 values: 528 bytes (e4m3 + UE8M0) and 288 bytes (e2m1 + e4m3)
+# ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §八 '版本漂移' and the §十 format
+# table: 512 fp8 values and 16 UE8M0 scales with the RoPE part quantised too;
+# the FP4 option, 512 e2m1 values two to a byte and 32 e4m3 scales; data first,
+# scales after; §三 'UE8M0': a power-of-two scale, rounded up)
+# ----------------------------------------------------------------------------
+V41_DIM = 512
+FP8_528_ROW_BYTES = 528
+FP4_288_ROW_BYTES = 288
+E2M1_MAX = 6.0
+
+
+def e2m1_value_table() -> np.ndarray:
+    """Value of each of the 16 e2m1 (FP4) codes, from the format's definition:
+    sign bit, 2 exponent bits with bias 1, 1 mantissa bit, no inf or NaN."""
+    vals = np.empty(16, dtype=np.float64)
+    for code in range(16):
+        sign = -1.0 if code & 0x8 else 1.0
+        e = (code >> 1) & 0x3
+        m = code & 0x1
+        vals[code] = sign * ((m / 2.0) if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1))
+    return vals
+
+
+def ue8m0_value(byte) -> np.ndarray:
+    """UE8M0 scale byte -> 2^(byte - 127); 0xFF is NaN."""
+    b = np.asarray(byte, dtype=np.int64)
+    return np.where(b == 255, np.nan, np.exp2((b - 127).astype(np.float64)))
+
+
+def _rows_bf16_f64(rows, width: int) -> np.ndarray:
+    """bf16 rows (torch tensor or uint16 bit patterns) [N, width] -> float64."""
+    import torch
+    if isinstance(rows, torch.Tensor):
+        assert rows.dtype == torch.bfloat16
+        bits = rows.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    else:
+        bits = np.asarray(rows, dtype=np.uint16)
+    assert bits.shape[-1] == width
+    return bf16_to_f64(bits.reshape(-1, width))
+
+
+def quantize_kv_fp8_528(rows) -> np.ndarray:
+    """bf16 rows [N, 512] -> uint8 [N, 528].
+
+    Per 32-value block j: amax = max |x|; the scale is the smallest power of
+    two 2^k, k >= -127, with 448 * 2^k >= amax (so no value saturates); byte
+    512 + j holds k + 127. Byte d holds e4m3_rne(x_d / 2^k), the division
+    being exact.
+    """
+    x = _rows_bf16_f64(rows, V41_DIM)
+    n = x.shape[0]
+    blocks = x.reshape(n, 16, 32)
+    amax = np.max(np.abs(blocks), axis=2)
+    ks = np.arange(-127, 128)
+    fits = E4M3_MAX * np.exp2(ks.astype(np.float64))[None, None, :] >= amax[:, :, None]
+    k = ks[np.argmax(fits, axis=2)]                    # first k that fits
+    y = blocks / np.exp2(k.astype(np.float64))[:, :, None]
+    out = np.empty((n, FP8_528_ROW_BYTES), dtype=np.uint8)
+    out[:, :V41_DIM] = e4m3_encode_rne(y.astype(np.float32)).reshape(n, V41_DIM)
+    out[:, V41_DIM:] = (k + 127).astype(np.uint8)
+    return out
+
+
+def dequantize_kv_fp8_528(raw: np.ndarray) -> np.ndarray:
+    """uint8 [N, 528] -> float64 [N, 512]: e4m3 value x 2^(byte - 127) of its
+    32-value block (exact in float64)."""
+    raw = np.ascontiguousarray(np.asarray(raw, dtype=np.uint8))
+    n = raw.shape[0]
+    vals = e4m3_value_table()[raw[:, :V41_DIM]].reshape(n, 16, 32)
+    scale = ue8m0_value(raw[:, V41_DIM:])
+    return (vals * scale[:, :, None]).reshape(n, V41_DIM)
+
+
+_E2M1_POS = e2m1_value_table()[:8]                     # 0, .5, 1, 1.5, 2, 3, 4, 6
+
+
+def e2m1_encode_rne(y: np.ndarray) -> np.ndarray:
+    """float64 values -> e2m1 codes: nearest magnitude, ties to the code with an
+    even last bit, magnitudes above 6 saturated to 6; the sign bit copied from
+    the input."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    hi = np.clip(np.searchsorted(_E2M1_POS, a, side="left"), 0, 7)
+    lo = np.clip(hi - 1, 0, 7)
+    d_lo = a - _E2M1_POS[lo]
+    d_hi = _E2M1_POS[hi] - a
+    code = np.where((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)), hi, lo)
+    code = np.where(a >= E2M1_MAX, 7, code)
+    return np.where(np.signbit(y), code | 0x8, code).astype(np.uint8)
+
+
+def quantize_kv_fp4_288(rows) -> np.ndarray:
+    """bf16 rows [N, 512] -> uint8 [N, 288].
+
+    Per 16-value block j: the scale is the smallest non-negative e4m3 value v
+    with 6 v >= amax (the block's largest value then needs no saturation), or
+    448 when no e4m3 value is large enough; byte 256 + j holds its code. Each
+    value becomes e2m1_rne(x / v) (0 with the sign of x when v = 0); byte i
+    holds value 2i in its low nibble and value 2i + 1 in its high nibble.
+    """
+    x = _rows_bf16_f64(rows, V41_DIM)
+    n = x.shape[0]
+    blocks = x.reshape(n, 32, 16)
+    amax = np.max(np.abs(blocks), axis=2)
+    fits = E2M1_MAX * _POS_VALUES[None, None, :] >= amax[:, :, None]   # codes 0x00..0x7E
+    sc = np.where(fits.any(axis=2), np.argmax(fits, axis=2), 0x7E).astype(np.uint8)
+    v = _POS_VALUES[sc]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(v[:, :, None] > 0, blocks / np.where(v > 0, v, 1.0)[:, :, None], 0.0 * blocks)
+    codes = e2m1_encode_rne(y).reshape(n, V41_DIM)
+    out = np.empty((n, FP4_288_ROW_BYTES), dtype=np.uint8)
+    out[:, :256] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    out[:, 256:] = sc
+    return out
+
+
+def dequantize_kv_fp4_288(raw: np.ndarray) -> np.ndarray:
+    """uint8 [N, 288] -> float64 [N, 512]: e2m1 value x the e4m3 scale of its
+    16-value block (exact in float64)."""
+    raw = np.ascontiguousarray(np.asarray(raw, dtype=np.uint8))
+    n = raw.shape[0]
+    codes = np.empty((n, V41_DIM), dtype=np.uint8)
+    codes[:, 0::2] = raw[:, :256] & 0xF
+    codes[:, 1::2] = raw[:, :256] >> 4
+    vals = e2m1_value_table()[codes].reshape(n, 32, 16)
+    scale = e4m3_value_table()[raw[:, 256:]]
+    return (vals * scale[:, :, None]).reshape(n, V41_DIM)
 
 
 # ----------------------------------------------------------------------------

@@ -188,6 +188,214 @@ def test_quantize_roundtrip_error_bound_and_fields():
 
 
 # ---------------------------------------------------------------------------
+# V4.1 rows of 512 values: 528 bytes (e4m3 + UE8M0) and 288 bytes (e2m1 + e4m3)
+# ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §八 '版本漂移', §十 format table)
+# ---------------------------------------------------------------------------
+def _golden_row(golden_dir, name):
+    codes, deq = [], []
+    for line in open(os.path.join(golden_dir, name)):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        kind, off, *vals = line.split()
+        if kind == "deq":
+            deq.append((int(off), float(vals[0])))
+        else:
+            codes.append((int(off), [int(v, 16) for v in vals]))
+    return codes, deq
+
+
+def _check_golden(raw, deq_row, codes, deq, data_bytes):
+    touched = np.zeros(data_bytes, bool)
+    for off, want in codes:
+        assert list(raw[off:off + len(want)]) == want, off
+        if off < data_bytes:
+            touched[off:off + len(want)] = True
+    assert (raw[:data_bytes][~touched] == 0).all()
+    for dim, v in deq:
+        assert deq_row[dim] == v and math.copysign(1, deq_row[dim]) == math.copysign(1, v), dim
+
+
+def test_fp8_528_golden_row(golden_dir):
+    row = np.zeros(512, np.float32)
+    row[0:4] = [1.0, -0.5, 0.3, 1.75]
+    row[32:34] = [3.0, -2.0 ** -12]
+    row[96] = 2.0 ** -16
+    row[128:130] = [57344.0, 100.0]
+    raw = oracle.quantize_kv_fp8_528(_bf16_bits(row)[None, :])[0]
+    assert raw.shape == (528,)
+    codes, deq = _golden_row(golden_dir, "fp8_528_row.txt")
+    _check_golden(raw, oracle.dequantize_kv_fp8_528(raw[None])[0], codes, deq, 512)
+
+
+def test_fp4_288_golden_row(golden_dir):
+    row = np.zeros(512, np.float32)
+    row[0:5] = [6.0, -1.0, 0.75, 2.5, 0.2]
+    row[16:18] = [7.0, -0.3125]
+    row[48:51] = [3072.0, 224.0, -1120.0]
+    row[64] = 0.01
+    raw = oracle.quantize_kv_fp4_288(_bf16_bits(row)[None, :])[0]
+    assert raw.shape == (288,)
+    codes, deq = _golden_row(golden_dir, "fp4_288_row.txt")
+    _check_golden(raw, oracle.dequantize_kv_fp4_288(raw[None])[0], codes, deq, 256)
+
+
+def test_v41_row_sizes():
+    """528 = 512 e4m3 + 16 UE8M0 (one per 32 values); 288 = 512 e2m1 at two
+    per byte + 32 e4m3 (one per 16 values) (拆解 §八, §十 table: 1/124 of the
+    MHA cache per token)."""
+    assert oracle.FP8_528_ROW_BYTES == 512 + 512 // 32 == 528
+    assert oracle.FP4_288_ROW_BYTES == 512 // 2 + 512 // 16 == 288
+
+
+def test_e2m1_table_is_the_format():
+    """FP4 e2m1 magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6 (the OCP
+    microscaling definition), negated under the sign bit."""
+    t = oracle.e2m1_value_table()
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(t[:8]) == mags
+    assert list(-t[8:]) == mags
+    assert math.copysign(1, t[8]) == -1
+    for c, v in enumerate(t):
+        assert oracle.e2m1_encode_rne(np.array([v]))[0] == c
+
+
+def test_ue8m0_values():
+    assert oracle.ue8m0_value(127) == 1.0
+    assert oracle.ue8m0_value(0) == 2.0 ** -127
+    assert oracle.ue8m0_value(254) == 2.0 ** 127
+    assert np.isnan(oracle.ue8m0_value(255))
+
+
+def _to_bf16_rows(x64):
+    t = torch.tensor(x64, dtype=torch.float64).to(torch.bfloat16)
+    assert (t.to(torch.float64).numpy() == x64).all()      # the test builds exact bf16 values
+    return t
+
+
+def test_fp8_528_grid_round_trip():
+    """Rows built from chosen codes and scales, with one +-448 per block so
+    that the chosen scale is the minimal one: quantising gives the bytes back."""
+    rng = _rng(40)
+    n = 24
+    table = oracle.e4m3_value_table()
+    finite = np.array([c for c in range(256) if not np.isnan(table[c])])
+    codes = rng.choice(finite, size=(n, 16, 32))
+    codes[:, :, 0] = rng.choice([0x7E, 0xFE], size=(n, 16))
+    k = rng.integers(-20, 8, size=(n, 16))
+    x = table[codes] * np.exp2(k.astype(np.float64))[:, :, None]
+    raw = oracle.quantize_kv_fp8_528(_to_bf16_rows(x.reshape(n, 512)))
+    np.testing.assert_array_equal(raw[:, :512], codes.reshape(n, 512).astype(np.uint8))
+    np.testing.assert_array_equal(raw[:, 512:], (k + 127).astype(np.uint8))
+    np.testing.assert_array_equal(oracle.dequantize_kv_fp8_528(raw), x.reshape(n, 512))
+
+
+def test_fp4_288_grid_round_trip():
+    """The same for the 288-byte rows: one +-6 per block makes the chosen
+    e4m3 scale the minimal one."""
+    rng = _rng(41)
+    n = 24
+    e2m1 = oracle.e2m1_value_table()
+    e4m3 = oracle.e4m3_value_table()
+    codes = rng.integers(0, 16, size=(n, 32, 16))
+    codes[:, :, 3] = rng.choice([7, 15], size=(n, 32))
+    sc = rng.integers(1, 0x7F, size=(n, 32))                # positive finite e4m3
+    x = e2m1[codes] * e4m3[sc][:, :, None]
+    raw = oracle.quantize_kv_fp4_288(_to_bf16_rows(x.reshape(n, 512)))
+    flat = codes.reshape(n, 512).astype(np.uint8)
+    np.testing.assert_array_equal(raw[:, :256], flat[:, 0::2] | (flat[:, 1::2] << 4))
+    np.testing.assert_array_equal(raw[:, 256:], sc.astype(np.uint8))
+    np.testing.assert_array_equal(oracle.dequantize_kv_fp4_288(raw), x.reshape(n, 512))
+
+
+def _blocks_of_mixed_magnitude(rng, n, width):
+    """bf16-exact rows whose blocks have magnitudes from 1e-30 to 1e30, with
+    exact ties planted."""
+    mag = 10.0 ** rng.uniform(-30, 30, size=(n, 512 // width, 1))
+    x = rng.standard_normal((n, 512 // width, width)) * mag
+    x[:, ::5, 1] = 0.0
+    return torch.tensor(x.reshape(n, 512)).to(torch.bfloat16)
+
+
+def test_fp8_528_brute_force():
+    """Per block, brute force in plain Python floats: the scale is the least
+    power of two that lets 448 cover amax, and each code is a nearest e4m3
+    value to x / 2^k (ties: even mantissa)."""
+    rng = _rng(42)
+    rows = _blocks_of_mixed_magnitude(rng, 6, 32)
+    raw = oracle.quantize_kv_fp8_528(rows)
+    x = rows.to(torch.float64).numpy().reshape(6, 16, 32)
+    table = [float(v) for v in oracle.e4m3_value_table()]
+    for r in range(6):
+        for j in range(16):
+            blk = [float(v) for v in x[r, j]]
+            amax = max(abs(v) for v in blk)
+            k = -127
+            while 448.0 * 2.0 ** k < amax:
+                k += 1
+            assert raw[r, 512 + j] == k + 127
+            for i, v in enumerate(blk):
+                y = v / 2.0 ** k
+                c = int(raw[r, 32 * j + i])
+                best = min(abs(t - y) for t in table if t == t)
+                assert abs(table[c] - y) == best
+                if best > 0:
+                    ties = [cc for cc in range(256) if table[cc] == table[cc] and abs(table[cc] - y) == best
+                            and (cc & 0x80) == (c & 0x80)]
+                    if len(ties) > 1:
+                        assert c % 2 == 0
+                assert (c & 0x80 != 0) == (math.copysign(1, v) < 0)
+
+
+def test_fp4_288_brute_force():
+    rng = _rng(43)
+    rows = _blocks_of_mixed_magnitude(rng, 6, 16)
+    rows[:, 7] = 2.0 ** -140          # a bf16 subnormal in a block
+    raw = oracle.quantize_kv_fp4_288(rows)
+    x = rows.to(torch.float64).numpy().reshape(6, 32, 16)
+    e4 = [float(v) for v in oracle.e4m3_value_table()[:0x7F]]
+    e2 = [float(v) for v in oracle.e2m1_value_table()]
+    for r in range(6):
+        for j in range(32):
+            blk = [float(v) for v in x[r, j]]
+            amax = max(abs(v) for v in blk)
+            ok = [c for c in range(0x7F) if 6.0 * e4[c] >= amax]
+            want_sc = ok[0] if ok else 0x7E
+            assert raw[r, 256 + j] == want_sc
+            v_sc = e4[want_sc]
+            for i, v in enumerate(blk):
+                d = 16 * j + i
+                c = int(raw[r, d // 2] >> (4 * (d % 2))) & 0xF
+                y = v / v_sc if v_sc > 0 else 0.0
+                dist = [abs(abs(e2[m]) - min(abs(y), 6.0)) for m in range(8)]
+                best = min(dist)
+                assert dist[c & 7] == best
+                if dist.count(best) > 1:
+                    assert (c & 7) % 2 == 0
+                assert (c >> 3) == (1 if math.copysign(1, v) < 0 else 0)
+
+
+def test_v41_quantise_error_bounds():
+    """|x - deq| is at most half a quantum: 2^(e-4) for e4m3 (e the binade of
+    x/2^k, at least -6) and half the e2m1 step times the scale for FP4,
+    wherever no saturation happens."""
+    rows = synth.make_latent_rows(32, seed=44, outlier_channels=4)[:, :512].contiguous()
+    x = oracle.to_f64(rows)
+    raw8 = oracle.quantize_kv_fp8_528(rows)
+    d8 = oracle.dequantize_kv_fp8_528(raw8)
+    k = raw8[:, 512:].astype(np.float64) - 127
+    y = x.reshape(32, 16, 32) / np.exp2(k)[:, :, None]
+    e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6)))
+    assert (np.abs(d8.reshape(32, 16, 32) - x.reshape(32, 16, 32)) <= np.exp2(e - 4 + k[:, :, None]) + 0).all()
+    raw4 = oracle.quantize_kv_fp4_288(rows)
+    d4 = oracle.dequantize_kv_fp4_288(raw4)
+    v = oracle.e4m3_value_table()[raw4[:, 256:]]
+    a = np.abs(x.reshape(32, 32, 16)) / v[:, :, None]
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))   # e2m1 spacing
+    assert (np.abs(d4.reshape(32, 32, 16) - x.reshape(32, 32, 16)) <= step / 2 * v[:, :, None]).all()
+
+
+# ---------------------------------------------------------------------------
 # attention: closed forms and brute force
 # ---------------------------------------------------------------------------
 def test_single_key_closed_form():
