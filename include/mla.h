@@ -53,14 +53,34 @@ typedef enum {
   MLA_ERR_INDEX = 4,            /* an out-of-range page or sparse index was skipped */
   MLA_ERR_TIMEOUT = 5,          /* a device pipeline wait gave up (kernel returned early) */
   MLA_ERR_CUDA = 6,             /* a CUDA runtime/driver call failed */
-  MLA_ERR_RANGE = 7             /* FP8 path: a value beyond fp16 range was saturated (see below) */
+  MLA_ERR_RANGE = 7             /* quantised cache: a value or a score beyond the certified range (see below) */
 } mla_status;
 
 typedef enum { MLA_DTYPE_BF16 = 0, MLA_DTYPE_FP16 = 1 } mla_dtype;
 
+/* Cache row formats (the `kv_format` argument; 0 and 1 are the reference's
+ * is_fp8_kvcache = false / true):
+ *  MLA_KV_16BIT    576 values of q_dtype (512 latent + 64 RoPE), 1152 B;
+ *  MLA_KV_FP8_656  512 e4m3 latent values, 4 fp32 scales (one per 128), the 64
+ *                  RoPE dims as bf16: 656 B ("FlashMLA 实战：MLA 注意力加速指南",
+ *                  §FP8 缓存怎么把 KV 压掉四成);
+ *  MLA_KV_FP8_528  the V4.1 row of 512 values (latent and RoPE together): 512
+ *                  e4m3 codes, then 16 UE8M0 scales, byte j = k + 127 for the
+ *                  scale 2^k of values [32j, 32j+32): 528 B;
+ *  MLA_KV_FP4_288  the FP4 row of 512 values: 256 bytes of e2m1 codes (value 2i
+ *                  in the low nibble of byte i), then 32 e4m3 scales, byte j for
+ *                  values [16j, 16j+16): 288 B
+ * ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §八 '版本漂移' and the §十
+ * format table). With the V4.1 rows a key is 512 wide and the value is the
+ * whole row: q is [batch, s_q, h_q, 512] and head_dim_v is 512. */
+typedef enum { MLA_KV_16BIT = 0, MLA_KV_FP8_656 = 1, MLA_KV_FP8_528 = 2, MLA_KV_FP4_288 = 3 } mla_kv_format;
+
 #define MLA_HEAD_DIM_K 576
 #define MLA_HEAD_DIM_V 512
 #define MLA_FP8_ROW_BYTES 656
+#define MLA_V41_DIM 512
+#define MLA_FP8_528_ROW_BYTES 528
+#define MLA_FP4_288_ROW_BYTES 288
 
 /* Human-readable name of a status code (static string). */
 MLA_API const char* mla_status_string(int status);
@@ -94,6 +114,7 @@ MLA_API size_t mla_metadata_size(int batch, int s_q, int num_sm_parts);
  * metadata      (device) mla_metadata_size() bytes, written.
  * num_splits    (device) int32 [batch*s_q + 1], written: exclusive prefix sum
  *               of the number of pieces of each virtual request.
+ * kv_format: an mla_kv_format, the one the decode calls will pass.
  * h_q must be 128, or 16 for dense 16-bit caches (the few-heads kernel);
  * h_kv must be 1, page_block 64.
  * Computed entirely on the device (no host synchronisation). The decode call
@@ -101,7 +122,7 @@ MLA_API size_t mla_metadata_size(int batch, int s_q, int num_sm_parts);
  * current cache_seqlens, and reports MLA_ERR_STALE_METADATA otherwise.
  */
 MLA_API mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int h_kv,
-                            int topk, int is_fp8, int causal, int page_block, int num_sm_parts,
+                            int topk, int kv_format, int causal, int page_block, int num_sm_parts,
                             void* metadata, int32_t* num_splits, void* stream);
 
 /* Bytes of decode workspace (status word, fp32 split partials, and one bit per
@@ -114,10 +135,13 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * cache_seqlens, head_dim_v=512, metadata, num_splits, softmax_scale, causal,
  * is_fp8_kvcache, indices)).
  *
- * q            (device) [batch, s_q, h_q, 576], `q_dtype`, contiguous, 16-B aligned.
- * kvcache      (device) [num_blocks, page_block, 1, 576] of q_dtype (is_fp8 = 0), or
- *              [num_blocks, page_block, 1, 656] uint8 rows (is_fp8 = 1, see
- *              mla_quantize_kv_fp8), contiguous, 16-B aligned.
+ * q            (device) [batch, s_q, h_q, 576] (V4.1 rows: 512), `q_dtype`,
+ *              contiguous, 16-B aligned; bf16 with every quantised format.
+ * kvcache      (device) [num_blocks, page_block, 1, row] contiguous, 16-B
+ *              aligned: 576 values of q_dtype (kv_format = MLA_KV_16BIT), or
+ *              uint8 rows of 656, 528 or 288 bytes (MLA_KV_FP8_656,
+ *              MLA_KV_FP8_528, MLA_KV_FP4_288; see the quantisers below).
+ *              Token-sparse decode (indices) reads the quantised formats.
  * block_table  (device) int32 [batch, max_blocks], logical page -> physical page;
  *              may be NULL when indices != NULL.
  * cache_seqlens(device) int32 [batch] tokens per request (ignored when indices != NULL).
@@ -137,7 +161,7 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  *              (query position, head) row that the combine recomputes exactly
  *              (the library leaves those bits zero after every call).
  * A request with no visible token gets out = 0 and lse = -inf.
- * FP8 caches (is_fp8 = 1) run the latent product in fp16: the bf16 query is
+ * 656-byte FP8 rows run the latent product in fp16: the bf16 query is
  * rounded to fp16 and each cache value is formed as fp16(code) x fp16(block
  * scale), rounded to fp16. Within range the dequantised value has relative
  * error <= 2^-10; a block whose amax is below 448 * 2^-14 (~0.027) has an
@@ -145,14 +169,17 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * instead. Out of range -- a query entry beyond 65504 in magnitude (saturated
  * to +-65504) or a block scale above 146 (block amax above 65408) -- the
  * status word records MLA_ERR_RANGE.
- * Every cache type splits the 576 dims of a score between the two CTAs of a
+ * The V4.1 rows run in bf16: e4m3 x 2^k and e2m1 x e4m3 are exact in bf16
+ * while the UE8M0 scale is at most 2^15 (byte 142; beyond it MLA_ERR_RANGE)
+ * and the value is at least 2^-126 (smaller ones may lose bits).
+ * Every cache type splits the dims of a score between the two CTAs of a
  * pair, which exchange fp16 factors 2^(partial score - partial max). The
  * result is certified exact (to fp16 precision) for a row of a 64-token tile
  * unless the two partial scores of its tokens disagree by more than about 22
  * binades; such a row is recomputed exactly from q and the cache rows for
  * 16-bit caches (by the combine step, so mla_decode_splitkv alone leaves it
  * uncorrected until mla_combine_splits runs), and reported as MLA_ERR_RANGE
- * for FP8 caches.
+ * for quantised caches.
  * h_q = 128 with any cache; h_q = 16 with a dense 16-bit cache only: the few
  * heads fill the MMA's N dimension and the 64 tokens of a tile its M
  * dimension, the transposed formulation S^T = K Q^T, O^T = V^T P^T of the
@@ -162,7 +189,7 @@ MLA_API mla_status mla_decode_with_kvcache(const void* q, int q_dtype, const voi
                                    int page_block, const int32_t* block_table, int max_blocks,
                                    const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                                    int head_dim_v, const void* metadata, const int32_t* num_splits,
-                                   int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                   int num_sm_parts, float softmax_scale, int causal, int kv_format,
                                    const int32_t* indices, int topk, void* out, float* lse,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
@@ -182,14 +209,14 @@ MLA_API mla_status mla_decode_splitkv(const void* q, int q_dtype, const void* kv
                                       int page_block, const int32_t* block_table, int max_blocks,
                                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                                       int head_dim_v, const void* metadata, const int32_t* num_splits,
-                                      int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                      int num_sm_parts, float softmax_scale, int causal, int kv_format,
                                       const int32_t* indices, int topk, void* out, float* lse,
                                       void* workspace, size_t workspace_bytes, void* stream);
 MLA_API mla_status mla_combine_splits(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
                                       int page_block, const int32_t* block_table, int max_blocks,
                                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                                       int head_dim_v, const void* metadata, const int32_t* num_splits,
-                                      int num_sm_parts, float softmax_scale, int causal, int is_fp8,
+                                      int num_sm_parts, float softmax_scale, int causal, int kv_format,
                                       const int32_t* indices, int topk, void* out, float* lse,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
@@ -214,7 +241,7 @@ MLA_API mla_status mla_combine_splits(const void* q, int q_dtype, const void* kv
  *    capture;
  *  - status (device, optional, 4-B aligned): receives the device-side status
  *    bits of this call (1 = index/page skipped, 2 = wait timeout, 4 = stale
- *    metadata, 8 = FP8 range), or NULL to discard them.
+ *    metadata, 8 = range of a quantised cache), or NULL to discard them.
  */
 MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, const void* kvcache,
                                                    int64_t num_blocks, int page_block,
@@ -222,7 +249,7 @@ MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, c
                                                    const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                                                    int head_dim_v, const void* metadata,
                                                    const int32_t* num_splits, int num_sm_parts,
-                                                   float softmax_scale, int causal, int is_fp8,
+                                                   float softmax_scale, int causal, int kv_format,
                                                    const int32_t* indices, int topk, void* out, float* lse,
                                                    uint32_t* status, void* stream);
 
@@ -236,6 +263,25 @@ MLA_API mla_status mla_decode_with_kvcache_noalloc(const void* q, int q_dtype, c
  * kv (device) bf16 [n, 576] (row stride 576 elements); out (device) uint8 [n, 656].
  */
 MLA_API mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* stream);
+
+/*
+ * Write the V4.1 rows of 512 values ("矩阵、注意力与 GPU：拆解 DeepGEMM 与
+ * FlashMLA", §八 '版本漂移', §十 format table; §三 'UE8M0': a power-of-two
+ * scale, rounded up). The page prints no quantiser; these follow the plainest
+ * reading of it, and the oracle defines the same decisions independently:
+ *  - mla_quantize_kv_fp8_528: per 32 values the scale is the smallest 2^k
+ *    (k >= -127) with 448 * 2^k >= amax; byte 512 + j = k + 127; byte d =
+ *    e4m3 round-to-nearest-even of x_d / 2^k (exact division);
+ *  - mla_quantize_kv_fp4_288: per 16 values the scale is the smallest
+ *    non-negative e4m3 value v with 6 v >= amax (448 when none is, values then
+ *    saturate to +-6); byte 256 + j = its code; each value becomes the e2m1
+ *    code nearest to x / v (ties to the even code, the sign of x kept), value
+ *    2i in the low nibble of byte i.
+ * kv (device) bf16 [n, 512] (row stride 512 elements, finite values); out
+ * (device) uint8 [n, 528] or [n, 288]; both 16-B aligned.
+ */
+MLA_API mla_status mla_quantize_kv_fp8_528(const void* kv, uint8_t* out, int64_t n, void* stream);
+MLA_API mla_status mla_quantize_kv_fp4_288(const void* kv, uint8_t* out, int64_t n, void* stream);
 
 /*
  * The per-head GEMMs around the kernel ("矩阵、注意力与 GPU：拆解 DeepGEMM 与
@@ -272,7 +318,7 @@ MLA_API mla_status mla_up_project(const void* o_lat, const void* w_uv, void* o_o
  * any 4-B status word, e.g. the one given to mla_absorb_q), and return the
  * first error it records, in the order timeout, stale metadata, index, range
  * (MLA_OK if none). *bits (optional) receives the raw bits: 1 = index/page
- * skipped, 2 = wait timeout, 4 = stale metadata, 8 = FP8 range.
+ * skipped, 2 = wait timeout, 4 = stale metadata, 8 = range of a quantised cache.
  */
 MLA_API mla_status mla_read_status(void* workspace, void* stream, uint32_t* bits);
 

@@ -66,8 +66,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
             f.argtypes = lib.mla_decode_with_kvcache.argtypes
         lib.mla_decode_with_kvcache_noalloc.restype = c.c_int
         lib.mla_decode_with_kvcache_noalloc.argtypes = lib.mla_decode_with_kvcache.argtypes[:-3] + [vp, vp]
-        lib.mla_quantize_kv_fp8.restype = c.c_int
-        lib.mla_quantize_kv_fp8.argtypes = [vp, vp, c.c_int64, vp]
+        for name in ("mla_quantize_kv_fp8", "mla_quantize_kv_fp8_528", "mla_quantize_kv_fp4_288"):
+            f = getattr(lib, name)
+            f.restype = c.c_int
+            f.argtypes = [vp, vp, c.c_int64, vp]
         lib.mla_read_status.restype = c.c_int
         lib.mla_read_status.argtypes = [vp, vp, c.POINTER(c.c_uint32)]
         for name in ("mla_absorb_q", "mla_up_project"):
@@ -120,11 +122,26 @@ class Metadata:
         self.key = key
 
 
+# cache row formats (the kv_format argument; is_fp8=True is KV_FP8_656)
+KV_16BIT, KV_FP8_656, KV_FP8_528, KV_FP4_288 = 0, 1, 2, 3
+ROW_WIDTH = {KV_16BIT: 576, KV_FP8_656: 576, KV_FP8_528: 512, KV_FP4_288: 512}   # query / key width
+
+
+def _kv_format(is_fp8: bool, kv_format: Optional[int]) -> int:
+    if kv_format is None:
+        return KV_FP8_656 if is_fp8 else KV_16BIT
+    if kv_format not in ROW_WIDTH:
+        raise MLAError(1, f"unknown kv_format {kv_format}")
+    return int(kv_format)
+
+
 def mla_get_metadata(cache_seqlens: Optional[torch.Tensor], s_q: int, h_q: int = 128, *, batch: Optional[int] = None,
                      topk: int = 0, is_fp8: bool = False, causal: bool = False, page_block: int = 64,
-                     num_sm_parts: Optional[int] = None, device=None) -> Tuple[Metadata, torch.Tensor]:
+                     num_sm_parts: Optional[int] = None, device=None,
+                     kv_format: Optional[int] = None) -> Tuple[Metadata, torch.Tensor]:
     """Compute the split-KV schedule on the device (no host sync)."""
     lib = load_library()
+    fmt = _kv_format(is_fp8, kv_format)
     if cache_seqlens is not None:
         batch = int(cache_seqlens.shape[0])
         device = cache_seqlens.device
@@ -135,10 +152,10 @@ def mla_get_metadata(cache_seqlens: Optional[torch.Tensor], s_q: int, h_q: int =
     nbytes = lib.mla_metadata_size(batch, s_q, parts)
     meta = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=device)
     num_splits = torch.empty(batch * s_q + 1, dtype=torch.int32, device=device)
-    st = lib.mla_get_metadata(_ptr(cache_seqlens), batch, s_q, h_q, 1, topk, int(is_fp8), int(causal), page_block,
+    st = lib.mla_get_metadata(_ptr(cache_seqlens), batch, s_q, h_q, 1, topk, fmt, int(causal), page_block,
                               parts, _ptr(meta), _ptr(num_splits), _stream(device))
     _check(st, "mla_get_metadata")
-    return Metadata(meta, num_splits, parts, (batch, s_q, h_q, topk, bool(is_fp8), bool(causal))), num_splits
+    return Metadata(meta, num_splits, parts, (batch, s_q, h_q, topk, fmt, bool(causal))), num_splits
 
 
 _ws_cache = {}
@@ -162,12 +179,15 @@ def mla_decode_with_kvcache(q: torch.Tensor, kvcache: torch.Tensor, block_table:
                             num_splits: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
                             causal: bool = False, is_fp8: bool = False, indices: Optional[torch.Tensor] = None,
                             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                            workspace: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, kv_format: Optional[int] = None,
                             _entry: str = "mla_decode_with_kvcache") -> Tuple[torch.Tensor, torch.Tensor]:
-    """out [B, s_q, h_q, 512] (q dtype), lse [B, s_q, h_q] fp32 (natural log)."""
+    """out [B, s_q, h_q, 512] (q dtype), lse [B, s_q, h_q] fp32 (natural log).
+    ``kv_format`` picks the cache row format (KV_*); q is [B, s_q, h_q, 576],
+    or 512 wide with the V4.1 rows (KV_FP8_528, KV_FP4_288)."""
     lib = load_library()
+    fmt = _kv_format(is_fp8, kv_format)
     B, s_q, h_q, d_k = q.shape
-    assert d_k == 576 and q.is_contiguous() and kvcache.is_contiguous()
+    assert d_k == ROW_WIDTH[fmt] and q.is_contiguous() and kvcache.is_contiguous()
     dev = _dev(q.device)
     num_blocks, page_block = int(kvcache.shape[0]), int(kvcache.shape[1])
     if softmax_scale is None:
@@ -186,7 +206,7 @@ def mla_decode_with_kvcache(q: torch.Tensor, kvcache: torch.Tensor, block_table:
     st = getattr(lib, _entry)(
         _ptr(q), DTYPE_CODES[q.dtype], _ptr(kvcache), num_blocks, page_block, _ptr(block_table), max_blocks,
         _ptr(cache_seqlens), B, s_q, h_q, head_dim_v, _ptr(metadata.meta), _ptr(num_splits), metadata.parts,
-        float(softmax_scale), int(causal), int(is_fp8), _ptr(indices), topk, _ptr(out), _ptr(lse), _ptr(workspace),
+        float(softmax_scale), int(causal), fmt, _ptr(indices), topk, _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel(), _stream(dev))
     _check(st, _entry)
     return out, lse
@@ -208,13 +228,15 @@ def mla_decode_with_kvcache_noalloc(q: torch.Tensor, kvcache: torch.Tensor, bloc
                                     causal: bool = False, is_fp8: bool = False,
                                     indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                                     lse: Optional[torch.Tensor] = None,
-                                    status: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                                    status: Optional[torch.Tensor] = None,
+                                    kv_format: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Decode using the library's fixed device scratch instead of a workspace
     (for callers that cannot allocate device memory on demand). ``out``/``lse``
     /``status`` are allocated here only when not given."""
     lib = load_library()
+    fmt = _kv_format(is_fp8, kv_format)
     B, s_q, h_q, d_k = q.shape
-    assert d_k == 576 and q.is_contiguous() and kvcache.is_contiguous()
+    assert d_k == ROW_WIDTH[fmt] and q.is_contiguous() and kvcache.is_contiguous()
     dev = _dev(q.device)
     num_blocks, page_block = int(kvcache.shape[0]), int(kvcache.shape[1])
     if softmax_scale is None:
@@ -230,7 +252,7 @@ def mla_decode_with_kvcache_noalloc(q: torch.Tensor, kvcache: torch.Tensor, bloc
     st = lib.mla_decode_with_kvcache_noalloc(
         _ptr(q), DTYPE_CODES[q.dtype], _ptr(kvcache), num_blocks, page_block, _ptr(block_table), max_blocks,
         _ptr(cache_seqlens), B, s_q, h_q, head_dim_v, _ptr(metadata.meta), _ptr(num_splits), metadata.parts,
-        float(softmax_scale), int(causal), int(is_fp8), _ptr(indices), topk, _ptr(out), _ptr(lse), _ptr(status),
+        float(softmax_scale), int(causal), fmt, _ptr(indices), topk, _ptr(out), _ptr(lse), _ptr(status),
         _stream(dev))
     _check(st, "mla_decode_with_kvcache_noalloc")
     return out, lse
@@ -246,6 +268,27 @@ def mla_quantize_kv_fp8(kv: torch.Tensor, out: Optional[torch.Tensor] = None) ->
     st = lib.mla_quantize_kv_fp8(_ptr(kv), _ptr(out), n, _stream(kv.device))
     _check(st, "mla_quantize_kv_fp8")
     return out
+
+
+def _quantize_v41(name: str, row_bytes: int, kv: torch.Tensor, out: Optional[torch.Tensor]) -> torch.Tensor:
+    lib = load_library()
+    assert kv.dtype == torch.bfloat16 and kv.shape[-1] == 512 and kv.is_contiguous()
+    n = kv.numel() // 512
+    if out is None:
+        out = torch.empty(*kv.shape[:-1], row_bytes, dtype=torch.uint8, device=kv.device)
+    st = getattr(lib, name)(_ptr(kv), _ptr(out), n, _stream(kv.device))
+    _check(st, name)
+    return out
+
+
+def mla_quantize_kv_fp8_528(kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """bf16 rows [..., 512] -> uint8 rows [..., 528] (V4.1: e4m3 + UE8M0 per 32)."""
+    return _quantize_v41("mla_quantize_kv_fp8_528", 528, kv, out)
+
+
+def mla_quantize_kv_fp4_288(kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """bf16 rows [..., 512] -> uint8 rows [..., 288] (e2m1 + e4m3 per 16)."""
+    return _quantize_v41("mla_quantize_kv_fp4_288", 288, kv, out)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

@@ -82,7 +82,13 @@
 namespace mla {
 namespace dense {
 
-enum : int { MODE_BF16 = 0, MODE_FP16 = 1, MODE_FP8 = 2, MODE_FP8_SPARSE = 3 };
+// 16-bit caches (576-wide rows); 656-byte FP8 rows; the V4.1 rows of 512
+// values: 528-byte FP8 (e4m3 + UE8M0 per 32) and 288-byte FP4 (e2m1 + e4m3
+// per 16); each quantised row format paged (dense) or token-sparse
+enum : int {
+  MODE_BF16 = 0, MODE_FP16 = 1, MODE_FP8 = 2, MODE_FP8_SPARSE = 3,
+  MODE_V41_FP8 = 4, MODE_V41_FP8_SPARSE = 5, MODE_V41_FP4 = 6, MODE_V41_FP4_SPARSE = 7
+};
 
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
@@ -111,21 +117,34 @@ constexpr float kCertify = 256.0f;
 constexpr uint32_t kXStride = 17 * 1024;
 constexpr uint32_t kEBar = 1;                           // named barrier of the 128 E-warp threads
 // FP8 rows (656 B): e4m3 [0,512), 4 fp32 scales [512,528), 64 bf16 RoPE [528,656)
-constexpr uint32_t kRawLat = 64 * 256;     // this CTA's 256 e4m3 per token
+// V4.1 FP8 rows (528 B): e4m3 [0,512), 16 UE8M0 scales [512,528)
+// V4.1 FP4 rows (288 B): e2m1 [0,256) (value 2i in the low nibble of byte i),
+// 32 e4m3 scales [256,288)
 
 // per-mode layout (offsets from a 1024-B aligned base) and barrier indices
 template <int kMode>
 struct Cfg {
   static constexpr bool kFp16 = kMode == MODE_FP16;
-  static constexpr bool kFp8 = kMode >= MODE_FP8;
-  static constexpr bool kSparse = kMode == MODE_FP8_SPARSE;
-  static constexpr int kNS = kSparse ? 3 : (kFp8 ? 3 : 5);  // KV ring slots (tiles)
-  // FP8: two more dequant warps (12, 13) and the P . V issuer (14)
-  static constexpr int kThreads = kFp8 ? 480 : 384;
-  static constexpr int kPvWarp = kFp8 ? 14 : 2;          // its lane 0 issues P . V
-  static constexpr int kRawNS = 3;                        // FP8 raw staging slots
-  // the 4 fp32 scales of each token: 16 B per row; the sparse gather writes
-  // them four rows (64 B) at a time into 128-B aligned units
+  static constexpr bool kQuant = kMode >= MODE_FP8;        // quantised rows: dequant warps
+  static constexpr bool kF656 = kMode == MODE_FP8 || kMode == MODE_FP8_SPARSE;
+  static constexpr bool kV41 = kMode >= MODE_V41_FP8;      // 512-value rows, no separate RoPE part
+  static constexpr bool kFp4 = kMode >= MODE_V41_FP4;
+  static constexpr bool kSparse = kMode == MODE_FP8_SPARSE || kMode == MODE_V41_FP8_SPARSE ||
+                                  kMode == MODE_V41_FP4_SPARSE;
+  // 16-bit operand type of the latent QK^T and P . V: bf16, except fp16 for
+  // fp16 caches and for 656-byte FP8 rows (whose products are formed in fp16)
+  static constexpr bool kLatBf16 = !(kFp16 || kF656);
+  static constexpr int kNS = kQuant ? 3 : 5;              // KV ring slots (tiles)
+  // quantised rows: two more dequant warps (12, 13) and the P . V issuer (14)
+  static constexpr int kThreads = kQuant ? 480 : 384;
+  static constexpr int kPvWarp = kQuant ? 14 : 2;         // its lane 0 issues P . V
+  static constexpr int kRawNS = 3;                        // raw staging slots
+  static constexpr uint32_t kRowBytes = kFp4 ? 288 : (kV41 ? 528 : 656);
+  static constexpr uint32_t kRawRow = kFp4 ? 128 : 256;   // this CTA's data bytes of a row
+  static constexpr uint32_t kRawLat = 64 * kRawRow;
+  // 16 scale bytes per row (656: the 4 fp32 scales; 528: the 16 UE8M0 scales;
+  // 288: this CTA's 16 e4m3 scales); the sparse gather writes them four rows
+  // (64 B) at a time into 128-B aligned units
   static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
   static constexpr uint32_t kRawSlot = kRawLat + kRawSc;
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
@@ -133,7 +152,7 @@ struct Cfg {
   static constexpr uint32_t OFF_QR = OFF_XS + kXStride;  // 32 RoPE dims of Q: 128 rows x 64 B
   static constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
   static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlot;
-  static constexpr uint32_t OFF_BAR = OFF_RAW + (kFp8 ? kRawNS * kRawSlot : 0);
+  static constexpr uint32_t OFF_BAR = OFF_RAW + (kQuant ? kRawNS * kRawSlot : 0);
   static constexpr uint32_t B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1,
                             B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SEMPTY + 1,
                             B_PEMPTY = B_PFULL + 2, B_OEMPTY = B_PEMPTY + 2, B_XFULL = B_OEMPTY + 1,
@@ -146,6 +165,7 @@ struct Cfg {
 };
 static_assert(Cfg<MODE_BF16>::kSmemBytes <= 232448, "shared memory");
 static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_V41_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
 
@@ -174,6 +194,30 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// four bytes of e2m1 pairs -> four f16 pairs (exact); byte i gives h[i], its
+// low nibble in the low half
+__device__ __forceinline__ void cvt_e2m1x4_f16x2(uint32_t w, uint32_t* h) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+// an f16 pair whose values are normal (or zero) with at most 7 significant
+// bits -> the bf16 pair of the same values times 2^-112: the 5-bit exponent
+// field moves into the low bits of bf16's 8-bit field (bias 15 read as bias
+// 127) and the mantissa loses only zero bits
+__device__ __forceinline__ uint32_t f16x2_as_bf16x2_m112(uint32_t h) {
+  return ((h & 0x7FFF7FFFu) >> 3) | (h & 0x80008000u);
+}
 
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads, 1)
@@ -181,9 +225,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
                       const __grid_constant__ CUtensorMap tm_kvr, const __grid_constant__ CUtensorMap tm_sc,
                       const DecodeParams p) {
   using C = Cfg<kMode>;
-  constexpr bool kFp16 = C::kFp16, kFp8 = C::kFp8, kSparse = C::kSparse;
+  constexpr bool kFp16 = C::kFp16, kQuant = C::kQuant, kF656 = C::kF656, kV41 = C::kV41, kFp4 = C::kFp4,
+                 kSparse = C::kSparse;
   constexpr int NS = C::kNS;
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
+  constexpr int kDQ = kV41 ? 512 : kDK;  // query row width
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -202,11 +248,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      // producer (+ the two dequant warps for FP8 caches)
-      mbar_init(bar(C::B_FULL + s), kFp8 ? 1 + kDequantWarps : 1);
+      // producer (RoPE part) and the dequant warps of quantised rows; V4.1
+      // rows have no separate RoPE part, so only the dequant warps fill a slot
+      mbar_init(bar(C::B_FULL + s), kV41 ? kDequantWarps : (kQuant ? 1 + kDequantWarps : 1));
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    mbar_init(bar(C::B_QFULL), kEWarps + 1);  // E warps (latent into TMEM) + RoPE TMA
+    mbar_init(bar(C::B_QFULL), kEWarps + 1);  // E warps (latent into TMEM) + producer (RoPE TMA)
     mbar_init(bar(C::B_QEMPTY), 1);
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_SEMPTY), kEWarps);
@@ -268,14 +315,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
   if (ok && warp == 0 && (kSparse || lane == 0)) {
     // ---------------- producer: RoPE dims of Q per piece, KV per tile ----------------
     if (lane == 0) {
-      prefetch_tmap(&tm_qr);
       prefetch_tmap(&tm_kv);
-      prefetch_tmap(&tm_kvr);
-      if constexpr (kFp8) prefetch_tmap(&tm_sc);
+      if constexpr (!kV41) {
+        prefetch_tmap(&tm_qr);
+        prefetch_tmap(&tm_kvr);
+      }
+      if constexpr (kQuant) prefetch_tmap(&tm_sc);
     }
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
     const int xr = 512 + 32 * (int)rank;  // RoPE column of this CTA (bf16 caches)
+    // byte column of the scales this CTA reads (288-byte rows: its own 16)
+    const int kScX = kFp4 ? 256 + 16 * (int)rank : 512;
     PieceIter it(p, part);
     Piece pc;
     int g = 0, qn = 0;
@@ -294,7 +345,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       if (lane == 0) {
         if (!wait(bar(C::B_QEMPTY), (qn & 1) ^ 1, guard)) stop = true;
-        else {
+        else if constexpr (kV41) {
+          mbar_arrive(bar(C::B_QFULL));  // no RoPE part: the E warps load all of Q
+        } else {
           mbar_arrive_expect_tx(bar(C::B_QFULL), 128 * 64);
           tma_load_2d(sb + C::OFF_QR, &tm_qr, bar(C::B_QFULL), xr, (b * p.s_q + i) * 128, pol_q);
           q_last = qn;
@@ -315,19 +368,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         if constexpr (!kSparse) {
           const int page = sane(pg_next);
           pg_next = raw_page(b, t + 1);
-          if constexpr (kFp8) {
-            // raw e4m3 + scales into the staging ring, converted by the dequant warps
+          if constexpr (kQuant) {
+            // raw codes + scales into the staging ring, converted by the dequant warps
             const int rs = g % C::kRawNS;
             if (!wait(bar(C::B_REMPTY + rs), ((g / C::kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
             const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
-            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), kRawLat + C::kRawSc);
-            tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), 256 * (int)rank, page * kTile, pol_kv);
-            tma_load_2d(raw + kRawLat, &tm_sc, bar(C::B_RFULL + rs), 512, page * kTile, pol_kv);
+            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), C::kRawLat + C::kRawSc);
+            tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), (int)C::kRawRow * (int)rank, page * kTile, pol_kv);
+            tma_load_2d(raw + C::kRawLat, &tm_sc, bar(C::B_RFULL + rs), kScX, page * kTile, pol_kv);
             last_rg[rs] = g;
+            if constexpr (kV41) continue;  // the dequant warps fill the whole operand slot
           }
           if (!wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard)) { stop = true; break; }
           const uint32_t slot = sb + C::OFF_RING + s * kSlot;
-          if constexpr (kFp8) {
+          if constexpr (kQuant) {
             // the RoPE dims are bf16 in the row: straight into the operand slot
             mbar_arrive_expect_tx(bar(C::B_FULL + s), kRChunk);
             tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), 528 + 64 * (int)rank, page * kTile, pol_kv);
@@ -339,9 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           last_g[s] = g;
         } else {
           // sparse: TMA gather4, four rows per copy; lane j < 16 fetches rows
-          // 4j .. 4j+3 of the tile for each of the three fields (this CTA's
-          // 256 e4m3 bytes, the 16 scale bytes, its 64 RoPE bytes). A row that
-          // is -1 or out of range is fetched as row 0 and masked later.
+          // 4j .. 4j+3 of the tile for each field (this CTA's data bytes, the
+          // 16 scale bytes, and for 656-byte rows its 64 RoPE bytes). A row
+          // that is -1 or out of range is fetched as row 0 and masked later.
           const int rs = g % C::kRawNS;
           const int idx[2] = {n0, n1};
           if (t + 1 < pc.t1) sparse_fetch(p, pc.v, t + 1, n0, n1);  // consumed next tile
@@ -357,14 +411,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             const int c = __shfl_sync(0xffffffffu, s1, row & 31);
             r[q] = row < 32 ? a : c;
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (256 + 16));
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (C::kRawRow + 16));
           __syncwarp();
           if (lane < 16) {
             const uint32_t fb = bar(C::B_RFULL + rs);
-            tma_gather4(raw + lane * 4 * 256, &tm_kv, fb, 256 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
-            tma_gather4(raw + kRawLat + lane * 128, &tm_sc, fb, 512, r[0], r[1], r[2], r[3], pol_kv);
+            tma_gather4(raw + lane * 4 * C::kRawRow, &tm_kv, fb, (int)C::kRawRow * (int)rank, r[0], r[1], r[2], r[3],
+                        pol_kv);
+            tma_gather4(raw + C::kRawLat + lane * 128, &tm_sc, fb, kScX, r[0], r[1], r[2], r[3], pol_kv);
           }
           last_rg[rs] = g;
+          if constexpr (kV41) continue;
           // the RoPE dims (bf16 in the row) go straight into the operand slot,
           // four rows per copy, 64-byte swizzled by the copy; the dequant
           // warps fill the latent part
@@ -395,19 +451,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         while (!mbar_try_wait(bar(C::B_QFULL), q_last & 1) && cycles() - t_0 < kDrainLimitCycles) {}
       }
     }
-  } else if (kFp8 && ok && (warp == 2 || warp == 3 || warp == 12 || warp == 13)) {
-    // ---------------- dequant: e4m3 x fp32 scale -> fp16 operand tiles ----------------
-    // (fp16 keeps 11 bits of the product; the latent QK^T and P.V of FP8
-    // caches run as fp16 x fp16, the RoPE QK^T stays bf16 x bf16)
+  } else if (kQuant && ok && (warp == 2 || warp == 3 || warp == 12 || warp == 13)) {
+    // ---------------- dequant: codes x block scale -> 16-bit operand tiles ----------------
+    // 656-byte rows: e4m3 x fp32 scale -> fp16 (fp16 keeps 11 bits of the
+    // product; their latent QK^T and P . V run as fp16 x fp16, the RoPE QK^T
+    // stays bf16 x bf16). V4.1 rows: e4m3 x 2^k and e2m1 x e4m3 are exact in
+    // bf16 and run as bf16 x bf16.
     const int tid = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..127 over the four warps
     PieceIter it(p, part);
     Piece pc;
     int g = 0;
     bool failed = false;
-    // largest block scale seen: a scale of at most 146 (block amax <= 65408)
-    // keeps its fp16 copy at most 146 (an fp16 value), so no product code x
-    // scale (|code| <= 448) exceeds fp16's 65504
+    // 656: largest block scale seen: a scale of at most 146 (block amax <=
+    // 65408) keeps its fp16 copy at most 146 (an fp16 value), so no product
+    // code x scale (|code| <= 448) exceeds fp16's 65504
     float sc_max = 0.f;
+    // 528: largest UE8M0 byte seen: up to 142 (k <= 15, block amax <= 448 *
+    // 2^15) the factor 2^(k+112) below is a bf16 value
+    uint32_t ue_max = 0u;
     while (!failed && it.next(pc)) {
       MaskStream<kSparse> ms;
       ms.start(p, pc);
@@ -421,28 +482,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
         const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
         const uint32_t slot = sb + C::OFF_RING + s * kSlot;
-        const float* scales = reinterpret_cast<const float*>(smem + C::OFF_RAW + rs * C::kRawSlot + kRawLat);
+        const uint8_t* scales = smem + C::OFF_RAW + rs * C::kRawSlot + C::kRawLat;
         // 64 rows x 32 units of 8 values; consecutive lanes take consecutive
-        // units of one row (conflict-free 8-B loads, 16-B swizzled stores)
+        // units of one row (conflict-free loads, 16-B swizzled stores)
 #pragma unroll 4
         for (int it2 = 0; it2 < 16; ++it2) {
           const int id = it2 * 128 + tid;
           const int row = id >> 5, unit = id & 31;
           uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
           if ((vmask >> row) & 1ull) {
-            uint32_t lo, hi;
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 256 + unit * 8));
-            // dense: 16 B per row; sparse: rows 4k..4k+3 share a 128-B unit
-            const int srow = kSparse ? (row >> 2) * 32 + (row & 3) * 4 : row * 4;
-            const float sc = scales[srow + 2 * rank + (unit >> 4)];
-            sc_max = fmaxf(sc_max, sc);
-            // e4m3 -> f16 is exact; the product rounds once more through the
-            // fp16 copy of the scale (both roundings are below 2^-11 relative)
-            const uint32_t sc2 = pack_f16x2(sc, sc);
-            w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)), sc2);
-            w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)), sc2);
-            w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)), sc2);
-            w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)), sc2);
+            // the row's 16 scale bytes: dense 16 B per row; sparse: rows
+            // 4k..4k+3 share a 128-B unit
+            const uint8_t* sc_row = scales + (kSparse ? (row >> 2) * 128 + (row & 3) * 16 : row * 16);
+            if constexpr (kFp4) {
+              // 8 e2m1 values (4 bytes) x this CTA's e4m3 scale of their 16:
+              // e2m1 -> f16 is exact, moved to bf16 x 2^-112 by a shift,
+              // times bf16(scale x 2^112): exact (at most 5 significant bits,
+              // magnitudes in [2^-10, 2688])
+              const uint32_t wd = ld_shared_u32(raw + row * 128 + unit * 4);
+              const uint32_t sc = sc_row[unit >> 1];
+              const float sv = __half2float(__ushort_as_half((uint16_t)(cvt_e4m3x2_f16x2((uint16_t)sc) & 0xFFFFu)));
+              const uint32_t sbf = __float_as_uint(sv * 0x1p112f) >> 16;
+              const uint32_t s2 = sbf | (sbf << 16);
+              uint32_t h[4];
+              cvt_e2m1x4_f16x2(wd, h);
+              w0 = mul_bf16x2(f16x2_as_bf16x2_m112(h[0]), s2);
+              w1 = mul_bf16x2(f16x2_as_bf16x2_m112(h[1]), s2);
+              w2 = mul_bf16x2(f16x2_as_bf16x2_m112(h[2]), s2);
+              w3 = mul_bf16x2(f16x2_as_bf16x2_m112(h[3]), s2);
+            } else {
+              uint32_t lo, hi;
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 256 + unit * 8));
+              if constexpr (kV41) {
+                // 8 e4m3 x 2^k (UE8M0 byte k + 127 of their 32 values): e4m3 ->
+                // f16 is exact, moved to bf16 x 2^-112 by a shift, times
+                // 2^(k+112) (exact while k <= 15)
+                const uint32_t ue = sc_row[8 * rank + (unit >> 2)];
+                ue_max = ue > ue_max ? ue : ue_max;
+                const uint32_t f = (ue + 112u) << 7;
+                const uint32_t f2 = f | (f << 16);
+                w0 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF))), f2);
+                w1 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16))), f2);
+                w2 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF))), f2);
+                w3 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16))), f2);
+              } else {
+                const float sc = reinterpret_cast<const float*>(sc_row)[2 * rank + (unit >> 4)];
+                sc_max = fmaxf(sc_max, sc);
+                // e4m3 -> f16 is exact; the product rounds once more through the
+                // fp16 copy of the scale (both roundings are below 2^-11 relative)
+                const uint32_t sc2 = pack_f16x2(sc, sc);
+                w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)), sc2);
+                w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)), sc2);
+                w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)), sc2);
+                w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)), sc2);
+              }
+            }
           }
           st_shared_v4(slot + (unit >> 3) * kKChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
         }
@@ -454,12 +548,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
       }
     }
-    if (__any_sync(0xffffffffu, !(sc_max <= 146.0f)) && lane == 0) atomicOr(p.status, STATUS_RANGE);
+    if (__any_sync(0xffffffffu, !(sc_max <= 146.0f) || ue_max > 142u) && lane == 0) atomicOr(p.status, STATUS_RANGE);
   } else if (ok && lane == 0 && (warp == 1 || warp == C::kPvWarp)) {
     // ---------------- UMMA issue ----------------
     // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
     // caches) and of the RoPE QK^T (the cache's RoPE dims: bf16 unless fp16)
-    constexpr bool kLatBf16 = !(kFp16 || kFp8);
+    constexpr bool kLatBf16 = C::kLatBf16;
     constexpr uint32_t idesc_qk = idesc_f16(128, 64, kLatBf16, false, false);
     constexpr uint32_t idesc_qr = idesc_f16(128, 64, !kFp16, false, false);
     constexpr uint32_t idesc_pv = idesc_f16(128, 256, kLatBf16, false, true);
@@ -480,8 +574,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           umma_ts(dS, tmem + kColQ + 32u * ci + 8u * k, d_k + (uint64_t)(ci * (kKChunk >> 4) + 2 * k), idesc_qk,
                   (ci | k) ? 1u : 0u);
       }
-      umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
-      umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
+      if constexpr (!kV41) {  // + this CTA's 32 RoPE dims
+        umma_ss(dS, d_qr, d_kr, idesc_qr, 1u);
+        umma_ss(dS, d_qr + 2, d_kr + 2, idesc_qr, 1u);
+      }
       umma_commit(bar(C::B_SFULL));
     };
     // O[:, this CTA's 256 dims] (+)= P V of tile g; frees P and the ring slot
@@ -565,7 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       if (q_idx > 0 && !warp_ok(wait(bar(C::B_QEMPTY), (q_idx - 1) & 1, guard))) return false;
       const int b = q_pc.v % p.batch, i = q_pc.v / p.batch;
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
-                                                        ((int64_t)(b * p.s_q + i) * 128 + h) * kDK + 256 * rank);
+                                                        ((int64_t)(b * p.s_q + i) * 128 + h) * kDQ + 256 * rank);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t r[64];
@@ -574,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           const uint4 x = __ldg(src + 16 * half + k);
           r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
         }
-        if constexpr (kFp8) {  // latent operands of FP8 caches are fp16
+        if constexpr (kF656) {  // latent operands of 656-byte FP8 rows are fp16
           float qmax = 0.f;
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
@@ -719,7 +815,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         auto prod = [&](int u) { return mul_f16x2_to_f32(eo[u], ep[u]); };
         float m_use, alpha, rs0;
         bool resc, cert;
-        if constexpr (!(kFp16 || kFp8)) {
+        if constexpr (C::kLatBf16) {
           // bf16 P keeps fp32's exponent range: the reference may sit far
           // above the tile's row max, so take mt and go in one pass
           const RowRef r(m, mt);
@@ -774,12 +870,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           // The halves disagree by more than about 22 binades on a row
           // (rare): the row's result from here on is not certified. For
           // 16-bit caches the row is flagged, and the combine kernel
-          // recomputes it exactly from q and the cache rows; FP8 caches report
-          // it. (Kept out of this kernel: its slow path would cost the common
+          // recomputes it exactly from q and the cache rows; quantised rows
+          // report it. (Kept out of this kernel: its slow path would cost the common
           // one registers and code.)
           const uint32_t unc = __ballot_sync(0xffffffffu, !cert);
           if (unc != 0u && rank == 0 && lane == 0) {
-            if constexpr (kFp8 || kSparse) atomicOr(p.status, STATUS_RANGE);
+            if constexpr (kQuant) atomicOr(p.status, STATUS_RANGE);
             else atomicOr(p.exact_flags + (int64_t)pc.v * 4 + (warp - 8), unc);
           }
         }
@@ -801,7 +897,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           }
           tmem_wait_st();
         }
-        if (!kFp8 && vm != ~0ull) {
+        if (!kQuant && vm != ~0ull) {
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
           // turn into NaN inside P . V (the dequant warps do this for FP8 rows)
           const uint32_t slot = sb + C::OFF_RING + (g % NS) * kSlot;

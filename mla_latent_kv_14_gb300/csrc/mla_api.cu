@@ -119,6 +119,10 @@ cudaError_t prepare_device(int dev) {
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP16>();
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8>();
     if (err == cudaSuccess) err = set_mode_smem<dense::MODE_FP8_SPARSE>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_V41_FP8>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_V41_FP8_SPARSE>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_V41_FP4>();
+    if (err == cudaSuccess) err = set_mode_smem<dense::MODE_V41_FP4_SPARSE>();
     if (err == cudaSuccess) err = set_smem(few::mla_decode_fewheads_kernel<false>, few::kSmemBytes);
     if (err == cudaSuccess) err = set_smem(few::mla_decode_fewheads_kernel<true>, few::kSmemBytes);
     if (err == cudaSuccess) {
@@ -163,7 +167,7 @@ const char* mla_status_string(int s) {
     case MLA_ERR_INDEX: return "out-of-range page or index skipped";
     case MLA_ERR_TIMEOUT: return "device pipeline wait timed out";
     case MLA_ERR_CUDA: return "CUDA error";
-    case MLA_ERR_RANGE: return "a value beyond the fp16 range of the FP8 path was saturated";
+    case MLA_ERR_RANGE: return "a value or score beyond the range a quantised cache path certifies";
     default: return "unknown status";
   }
 }
@@ -197,17 +201,18 @@ size_t mla_workspace_size(int batch, int s_q, int h_q, int parts) {
 }
 
 mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int h_kv, int topk,
-                            int is_fp8, int causal, int page_block, int parts, void* metadata, int32_t* num_splits,
+                            int kv_format, int causal, int page_block, int parts, void* metadata, int32_t* num_splits,
                             void* stream) {
   if (batch <= 0 || s_q <= 0 || parts <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_format < MLA_KV_16BIT || kv_format > MLA_KV_FP4_288) return MLA_ERR_INVALID_ARG;
   if (h_kv != 1 || page_block != kTile) return MLA_ERR_INVALID_ARG;
   if (h_q != 128 && h_q != kFewHeads) return MLA_ERR_UNSUPPORTED;
-  if (h_q == kFewHeads && (topk > 0 || is_fp8)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
+  if (h_q == kFewHeads && (topk > 0 || kv_format)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
   if (!metadata || !num_splits) return MLA_ERR_INVALID_ARG;
   if (topk == 0 && !cache_seqlens) return MLA_ERR_INVALID_ARG;
   if (topk > 0 && causal) return MLA_ERR_INVALID_ARG;
   if ((int64_t)batch * s_q > kMaxVreq) return MLA_ERR_UNSUPPORTED;
-  MetaParams mp{topk > 0 ? nullptr : cache_seqlens, batch, s_q, h_q, topk, is_fp8 ? 1 : 0, causal ? 1 : 0,
+  MetaParams mp{topk > 0 ? nullptr : cache_seqlens, batch, s_q, h_q, topk, kv_format, causal ? 1 : 0,
                 page_block, parts, static_cast<int32_t*>(metadata), num_splits};
   const size_t smem = metadata_smem_bytes(batch * s_q);
   if (smem > 48 * 1024) {
@@ -239,16 +244,40 @@ mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, in
 namespace {
 enum : int { STAGE_SPLIT = 1, STAGE_COMBINE = 2 };
 
+template <int kMode>
+cudaError_t launch_mode(cudaLaunchConfig_t cfg, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const CUtensorMap& d, const DecodeParams& p) {
+  cfg.blockDim = dim3(dense::Cfg<kMode>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dense::Cfg<kMode>::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<kMode>, a, b, c, d, p);
+}
+
+// the 128-head decode kernel of one cache format / addressing mode
+cudaError_t launch_decode_mode(int mode, const cudaLaunchConfig_t& cfg, const CUtensorMap& a, const CUtensorMap& b,
+                               const CUtensorMap& c, const CUtensorMap& d, const DecodeParams& p) {
+  switch (mode) {
+    case dense::MODE_BF16: return launch_mode<dense::MODE_BF16>(cfg, a, b, c, d, p);
+    case dense::MODE_FP16: return launch_mode<dense::MODE_FP16>(cfg, a, b, c, d, p);
+    case dense::MODE_FP8: return launch_mode<dense::MODE_FP8>(cfg, a, b, c, d, p);
+    case dense::MODE_FP8_SPARSE: return launch_mode<dense::MODE_FP8_SPARSE>(cfg, a, b, c, d, p);
+    case dense::MODE_V41_FP8: return launch_mode<dense::MODE_V41_FP8>(cfg, a, b, c, d, p);
+    case dense::MODE_V41_FP8_SPARSE: return launch_mode<dense::MODE_V41_FP8_SPARSE>(cfg, a, b, c, d, p);
+    case dense::MODE_V41_FP4: return launch_mode<dense::MODE_V41_FP4>(cfg, a, b, c, d, p);
+    default: return launch_mode<dense::MODE_V41_FP4_SPARSE>(cfg, a, b, c, d, p);
+  }
+}
+
 // Host-side argument checks of a decode call; nothing is enqueued. The
 // workspace is checked only when the caller supplies one (check_ws).
 mla_status validate_decode(const void* q, int q_dtype, const void* kvcache, int64_t num_blocks, int page_block,
                            const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens, int batch,
                            int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
-                           int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+                           int parts, float softmax_scale, int causal, int kv_format, const int32_t* indices, int topk,
                            void* out, float* lse, bool check_ws, void* workspace, size_t workspace_bytes) {
   if (!q || !kvcache || !out || !lse || (check_ws && !workspace) || !metadata || !num_splits)
     return MLA_ERR_INVALID_ARG;
   if (q_dtype != MLA_DTYPE_BF16 && q_dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
+  if (kv_format < MLA_KV_16BIT || kv_format > MLA_KV_FP4_288) return MLA_ERR_INVALID_ARG;
   if (head_dim_v != kDV || page_block != kTile) return MLA_ERR_INVALID_ARG;
   if (batch <= 0 || s_q <= 0 || parts <= 0 || num_blocks <= 0 || topk < 0) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
@@ -261,9 +290,9 @@ mla_status validate_decode(const void* q, int q_dtype, const void* kvcache, int6
   if (check_ws && workspace_bytes < mla_workspace_size(batch, s_q, h_q, parts)) return MLA_ERR_INVALID_ARG;
   if (num_blocks * (int64_t)page_block >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
   if (h_q != 128 && h_q != kFewHeads) return MLA_ERR_UNSUPPORTED;
-  if (h_q == kFewHeads && (indices || is_fp8)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
-  if (indices && !is_fp8) return MLA_ERR_UNSUPPORTED;                 // token-sparse decode reads FP8 rows
-  if (is_fp8 && q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED; // FP8 rows pair with bf16 queries
+  if (h_q == kFewHeads && (indices || kv_format)) return MLA_ERR_UNSUPPORTED;  // few heads: dense 16-bit caches
+  if (indices && !kv_format) return MLA_ERR_UNSUPPORTED;                 // token-sparse decode reads quantised rows
+  if (kv_format && q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED; // quantised rows pair with bf16 queries
   const int64_t qrows = (int64_t)batch * s_q * h_q;
   if (qrows >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
@@ -272,12 +301,12 @@ mla_status validate_decode(const void* q, int q_dtype, const void* kvcache, int6
 mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcache, int64_t num_blocks,
                        int page_block, const int32_t* block_table, int max_blocks, const int32_t* cache_seqlens,
                        int batch, int s_q, int h_q, int head_dim_v, const void* metadata, const int32_t* num_splits,
-                       int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+                       int parts, float softmax_scale, int causal, int kv_format, const int32_t* indices, int topk,
                        void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   // ---- host-side argument checks (nothing is enqueued on failure) ----
   const mla_status v = validate_decode(q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks,
                                        cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
-                                       softmax_scale, causal, is_fp8, indices, topk, out, lse, true, workspace,
+                                       softmax_scale, causal, kv_format, indices, topk, out, lse, true, workspace,
                                        workspace_bytes);
   if (v != MLA_OK) return v;
   const int64_t qrows = (int64_t)batch * s_q * h_q;
@@ -288,13 +317,19 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   MLA_CUDA(prepare_device(dev));
 
   const bool fp16 = q_dtype == MLA_DTYPE_FP16;
-  const int mode = is_fp8 ? (indices ? dense::MODE_FP8_SPARSE : dense::MODE_FP8)
-                          : (fp16 ? dense::MODE_FP16 : dense::MODE_BF16);
+  const bool sparse = indices != nullptr;
+  const bool v41 = kv_format == MLA_KV_FP8_528 || kv_format == MLA_KV_FP4_288;
+  int mode = fp16 ? dense::MODE_FP16 : dense::MODE_BF16;
+  if (kv_format == MLA_KV_FP8_656) mode = sparse ? dense::MODE_FP8_SPARSE : dense::MODE_FP8;
+  if (kv_format == MLA_KV_FP8_528) mode = sparse ? dense::MODE_V41_FP8_SPARSE : dense::MODE_V41_FP8;
+  if (kv_format == MLA_KV_FP4_288) mode = sparse ? dense::MODE_V41_FP4_SPARSE : dense::MODE_V41_FP4;
   const CUtensorMapDataType dt = fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t kvrows = (uint64_t)(num_blocks * page_block);
   // Q: the 32-dim RoPE halves (64-B swizzle). KV, 16-bit caches: 64-dim latent
   // chunks (128-B swizzle) and 32-dim RoPE halves (64-B swizzle). KV, FP8 rows
   // (bytes): 256 e4m3 per CTA, the 16 scale bytes, 64 RoPE bytes (64-B swizzle).
+  // V4.1 rows (bytes): this CTA's data bytes (256 e4m3 or 128 of e2m1 pairs)
+  // and 16 scale bytes; their queries are read by the kernel without a map.
   CUtensorMap tm_qr, tm_kv, tm_kvr, tm_sc;
   const bool few_heads = h_q == kFewHeads;
   if (few_heads) {
@@ -304,10 +339,19 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
         !make_map_chunks(&tm_kv, kvcache, dt, kvrows, 64, 9))
       return MLA_ERR_CUDA;
     tm_kvr = tm_sc = tm_kv;
-  } else if (!make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
+  } else if (!v41 && !make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return MLA_ERR_CUDA;
   }
   if (few_heads) {
+  } else if (v41) {
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int rb = kv_format == MLA_KV_FP4_288 ? kRowBytesFp4_288 : kRowBytesFp8_528;
+    const int data = kv_format == MLA_KV_FP4_288 ? 128 : 256;
+    const int box_rows = sparse ? 1 : 64;  // sparse: TMA gather4, one-row boxes
+    if (!make_map(&tm_kv, kvcache, u8, 1, kvrows, rb, rb, data, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_sc, kvcache, u8, 1, kvrows, rb, rb, 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MLA_ERR_CUDA;
+    tm_qr = tm_kvr = tm_kv;  // not read
   } else if (mode == dense::MODE_FP8_SPARSE) {
     // rows gathered four at a time (TMA gather4: one-row boxes, no swizzle):
     // this CTA's 256 e4m3 bytes, the 16 scale bytes, its 64 RoPE bytes
@@ -354,7 +398,7 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   p.h_q = h_q;
   p.topk = topk;
   p.causal = causal ? 1 : 0;
-  p.is_fp8 = is_fp8 ? 1 : 0;
+  p.kv_format = kv_format;
   p.parts = parts;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.stall_cycles = g_test_stall.load(std::memory_order_relaxed);
@@ -382,33 +426,14 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     cfg.gridDim = dim3(2 * parts, 1, 1);
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(is_fp8 ? dense::Cfg<dense::MODE_FP8>::kThreads : dense::kThreads, 1, 1);
     cfg.stream = st;
-    switch (mode) {
-      case dense::MODE_BF16:
-        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_BF16>::kSmemBytes;
-        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_BF16>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
-        break;
-      case dense::MODE_FP16:
-        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP16>::kSmemBytes;
-        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP16>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
-        break;
-      case dense::MODE_FP8:
-        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP8>::kSmemBytes;
-        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP8>, tm_qr, tm_kv, tm_kvr, tm_sc, p));
-        break;
-      default:
-        cfg.dynamicSmemBytes = dense::Cfg<dense::MODE_FP8_SPARSE>::kSmemBytes;
-        MLA_CUDA(cudaLaunchKernelEx(&cfg, dense::mla_decode_kernel<dense::MODE_FP8_SPARSE>, tm_qr, tm_kv, tm_kvr,
-                                    tm_sc, p));
-        break;
-    }
+    MLA_CUDA(launch_decode_mode(mode, cfg, tm_qr, tm_kv, tm_kvr, tm_sc, p));
   }
   if (!(stages & STAGE_COMBINE)) return MLA_OK;
 
   // combine, overlapped with the decode grid's tail (programmatic dependent launch)
   CombineParams c{num_splits, p.o_part, p.lse_part, out, lse, batch, s_q, h_q, fp16 ? 1 : 0};
-  if (!is_fp8 && !indices && h_q == 128) {  // the kernels that flag rows for an exact recompute
+  if (kv_format == MLA_KV_16BIT && !indices && h_q == 128) {  // the kernels that flag rows for an exact recompute
     c.exact_flags = p.exact_flags;
     c.q = q;
     c.kv = p.kv;
@@ -440,12 +465,12 @@ extern "C" {
 
 #define MLA_DECODE_ARGS                                                                                        \
   q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks, cache_seqlens, batch, s_q, h_q,         \
-      head_dim_v, metadata, num_splits, parts, softmax_scale, causal, is_fp8, indices, topk, out, lse, workspace, \
+      head_dim_v, metadata, num_splits, parts, softmax_scale, causal, kv_format, indices, topk, out, lse, workspace, \
       workspace_bytes, stream
 #define MLA_DECODE_PARAMS                                                                                         \
   const void *q, int q_dtype, const void *kvcache, int64_t num_blocks, int page_block, const int32_t *block_table, \
       int max_blocks, const int32_t *cache_seqlens, int batch, int s_q, int h_q, int head_dim_v,                   \
-      const void *metadata, const int32_t *num_splits, int parts, float softmax_scale, int causal, int is_fp8,     \
+      const void *metadata, const int32_t *num_splits, int parts, float softmax_scale, int causal, int kv_format,     \
       const int32_t *indices, int topk, void *out, float *lse, void *workspace, size_t workspace_bytes,            \
       void *stream
 
@@ -467,6 +492,32 @@ mla_status mla_quantize_kv_fp8(const void* kv, uint8_t* out, int64_t n, void* st
   mla_quant_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(kv), out, n);
   MLA_CUDA(cudaGetLastError());
   return MLA_OK;
+}
+
+static mla_status quantize_v41(const void* kv, uint8_t* out, int64_t n, bool fp4, void* stream) {
+  if (n < 0 || (n > 0 && (!kv || !out))) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  int dev = 0, sms = 0;
+  MLA_CUDA(cudaGetDevice(&dev));
+  MLA_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t want = (n + 7) / 8;  // one warp per row, 8 warps per block
+  const int grid = (int)(want < (int64_t)sms * 16 ? want : (int64_t)sms * 16);
+  const uint16_t* src = static_cast<const uint16_t*>(kv);
+  if (fp4)
+    mla_quant_fp4_288_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(src, out, n);
+  else
+    mla_quant_fp8_528_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(src, out, n);
+  MLA_CUDA(cudaGetLastError());
+  return MLA_OK;
+}
+
+mla_status mla_quantize_kv_fp8_528(const void* kv, uint8_t* out, int64_t n, void* stream) {
+  return quantize_v41(kv, out, n, false, stream);
+}
+
+mla_status mla_quantize_kv_fp4_288(const void* kv, uint8_t* out, int64_t n, void* stream) {
+  return quantize_v41(kv, out, n, true, stream);
 }
 
 mla_status mla_absorb_q(const void* q_nope, const void* w_uk, void* q_out, int tokens, int h_q, int dtype,
@@ -599,7 +650,7 @@ void* static_ws_ptr(int dev, cudaError_t* err) {
 extern "C" mla_status mla_decode_with_kvcache_noalloc(
     const void* q, int q_dtype, const void* kvcache, int64_t num_blocks, int page_block, const int32_t* block_table,
     int max_blocks, const int32_t* cache_seqlens, int batch, int s_q, int h_q, int head_dim_v, const void* metadata,
-    const int32_t* num_splits, int parts, float softmax_scale, int causal, int is_fp8, const int32_t* indices, int topk,
+    const int32_t* num_splits, int parts, float softmax_scale, int causal, int kv_format, const int32_t* indices, int topk,
     void* out, float* lse, uint32_t* status, void* stream) {
   const size_t need = mla_workspace_size(batch, s_q, h_q, parts);
   if (need == 0) return MLA_ERR_INVALID_ARG;
@@ -609,7 +660,7 @@ extern "C" mla_status mla_decode_with_kvcache_noalloc(
   // memset); the fixed array is the workspace, sized and aligned above
   const mla_status v = validate_decode(q, q_dtype, kvcache, num_blocks, page_block, block_table, max_blocks,
                                        cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
-                                       softmax_scale, causal, is_fp8, indices, topk, out, lse, false, nullptr, 0);
+                                       softmax_scale, causal, kv_format, indices, topk, out, lse, false, nullptr, 0);
   if (v != MLA_OK) return v;
   int dev = 0;
   MLA_CUDA(cudaGetDevice(&dev));
@@ -623,7 +674,7 @@ extern "C" mla_status mla_decode_with_kvcache_noalloc(
   MLA_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), st));
   mla_status r = decode_impl(STAGE_SPLIT | STAGE_COMBINE, q, q_dtype, kvcache, num_blocks, page_block, block_table,
                              max_blocks, cache_seqlens, batch, s_q, h_q, head_dim_v, metadata, num_splits, parts,
-                             softmax_scale, causal, is_fp8, indices, topk, out, lse, ws, kStaticWsBytes, stream);
+                             softmax_scale, causal, kv_format, indices, topk, out, lse, ws, kStaticWsBytes, stream);
   // device-side problems (bad index or page, stale metadata, wait timeout) are
   // recorded in the array's status word; copy them out for the caller
   if (r == MLA_OK && status) MLA_CUDA(cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st));

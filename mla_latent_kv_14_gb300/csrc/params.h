@@ -9,12 +9,15 @@ constexpr int kTile = 64;         // tokens per KV tile (= page_block)
 constexpr int kDK = 576;          // latent 512 + RoPE 64
 constexpr int kDV = 512;
 constexpr int kRowBytesFp8 = 656;
+constexpr int kDV41 = 512;        // V4.1 rows: 512 values (latent and RoPE together)
+constexpr int kRowBytesFp8_528 = 528;
+constexpr int kRowBytesFp4_288 = 288;
 constexpr int kPieceOverhead = 2; // schedule cost of starting a piece, in tiles
 
 // ---- metadata (int32 words) ----
 // header
 enum : int {
-  H_MAGIC = 0, H_BATCH, H_SQ, H_HQ, H_TOPK, H_FP8, H_CAUSAL, H_PAGE, H_PARTS, H_HASH,
+  H_MAGIC = 0, H_BATCH, H_SQ, H_HQ, H_TOPK, H_KVFMT, H_CAUSAL, H_PAGE, H_PARTS, H_HASH,
   H_NPIECES, H_VREQ, H_WORDS = 16
 };
 constexpr int32_t kMetaMagic = 0x31414C4D;  // "MLA1"
@@ -52,7 +55,7 @@ __host__ __device__ inline size_t ws_bytes(int vreq, int parts, int h_q) {
 
 struct MetaParams {
   const int32_t* seqlens;   // [batch] or null (sparse)
-  int batch, s_q, h_q, topk, is_fp8, causal, page_block, parts;
+  int batch, s_q, h_q, topk, kv_format, causal, page_block, parts;
   int32_t* meta;
   int32_t* split_off;       // [vreq + 1]
 };
@@ -74,7 +77,7 @@ struct DecodeParams {
   int64_t num_blocks;
   int64_t num_rows;            // num_blocks * page_block
   int max_blocks;
-  int batch, s_q, h_q, topk, causal, is_fp8, parts;
+  int batch, s_q, h_q, topk, causal, kv_format, parts;
   int out_v8;                  // out is 32-B aligned: 32-byte stores in the epilogue
   float scale_log2;            // softmax_scale * log2(e)
   // test hook, 0 in normal use: before any copy is issued, thread 0 of each CTA

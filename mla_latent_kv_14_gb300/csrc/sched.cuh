@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p
     h[H_SQ] = p.s_q;
     h[H_HQ] = p.h_q;
     h[H_TOPK] = p.topk;
-    h[H_FP8] = p.is_fp8;
+    h[H_KVFMT] = p.kv_format;
     h[H_CAUSAL] = p.causal;
     h[H_PAGE] = p.page_block;
     h[H_PARTS] = p.parts;
@@ -218,7 +218,7 @@ __host__ __device__ inline size_t metadata_smem_bytes(int vreq) {
 __device__ __forceinline__ bool metadata_matches(const DecodeParams& p, int page_block, uint32_t fp) {
   const int32_t* h = p.meta;
   return h[H_MAGIC] == kMetaMagic && h[H_BATCH] == p.batch && h[H_SQ] == p.s_q && h[H_HQ] == p.h_q &&
-         h[H_TOPK] == p.topk && h[H_FP8] == p.is_fp8 && h[H_CAUSAL] == p.causal && h[H_PAGE] == page_block &&
+         h[H_TOPK] == p.topk && h[H_KVFMT] == p.kv_format && h[H_CAUSAL] == p.causal && h[H_PAGE] == page_block &&
          h[H_PARTS] == p.parts && h[H_VREQ] == p.batch * p.s_q && (uint32_t)h[H_HASH] == fp;
 }
 
@@ -227,7 +227,7 @@ __device__ __forceinline__ bool metadata_matches(const DecodeParams& p, int page
 __device__ __forceinline__ bool header_matches(const int32_t (&h)[H_WORDS], const DecodeParams& p, int page_block,
                                                uint32_t fp) {
   return (h[H_MAGIC] == kMetaMagic) & (h[H_BATCH] == p.batch) & (h[H_SQ] == p.s_q) & (h[H_HQ] == p.h_q) &
-         (h[H_TOPK] == p.topk) & (h[H_FP8] == p.is_fp8) & (h[H_CAUSAL] == p.causal) & (h[H_PAGE] == page_block) &
+         (h[H_TOPK] == p.topk) & (h[H_KVFMT] == p.kv_format) & (h[H_CAUSAL] == p.causal) & (h[H_PAGE] == page_block) &
          (h[H_PARTS] == p.parts) & (h[H_VREQ] == p.batch * p.s_q) & ((uint32_t)h[H_HASH] == fp);
 }
 

@@ -41,15 +41,16 @@ def uniform_seqlens(batch: int, lo: int, hi: int, seed: int = 2) -> np.ndarray:
 
 def make_latent_rows(n_rows: int, dtype=torch.bfloat16, seed: int = 0,
                      outlier_channels: int = 0, outlier_gain: float = 8.0,
-                     device="cpu") -> torch.Tensor:
-    """``n_rows`` x 576 cache rows ~ N(0,1) in ``dtype``.
+                     device="cpu", d_k: int = D_K) -> torch.Tensor:
+    """``n_rows`` x ``d_k`` cache rows ~ N(0,1) in ``dtype`` (576, or 512 for
+    the V4.1 rows whose 512 values hold latent and RoPE together).
 
     With ``outlier_channels`` > 0, that many seeded latent channels of every
     row (distinct, in [0, 512)) are multiplied by ``outlier_gain`` before the
     rounding to ``dtype``.
     """
     g = _gen(seed, device)
-    x = torch.randn(n_rows, D_K, generator=g, device=device, dtype=torch.float32)
+    x = torch.randn(n_rows, d_k, generator=g, device=device, dtype=torch.float32)
     if outlier_channels > 0:
         go = _gen(seed + 4, device)
         # per-row distinct channels: top-k of a random key per (row, channel)
@@ -86,15 +87,15 @@ class DenseCase:
         return int(self.kv_rows.shape[0]) // self.page_block
 
     def kvcache_paged(self) -> torch.Tensor:
-        """The cache viewed as [num_blocks, page_block, 1, 576]."""
-        return self.kv_rows.view(self.num_blocks, self.page_block, 1, D_K)
+        """The cache viewed as [num_blocks, page_block, 1, d_k]."""
+        return self.kv_rows.view(self.num_blocks, self.page_block, 1, self.kv_rows.shape[1])
 
 
 def make_dense_case(seqlens: Sequence[int], s_q: int = 1, h_q: int = 128,
                     page_block: int = 64, dtype=torch.bfloat16, causal: bool = False,
                     seed: int = 0, spare_blocks: int = 0, shuffle: bool = True,
                     outlier_channels: int = 0, tail_fill: Optional[float] = None,
-                    device="cpu") -> DenseCase:
+                    device="cpu", d_k: int = D_K) -> DenseCase:
     """A paged dense-decode problem.
 
     Pages: each request gets ceil(L/page_block) pages (at least one) plus
@@ -118,7 +119,7 @@ def make_dense_case(seqlens: Sequence[int], s_q: int = 1, h_q: int = 128,
         bt[b, :pages[b]] = perm[cursor:cursor + pages[b]]
         cursor += pages[b]
     kv = make_latent_rows(total_pages * page_block, dtype=dtype, seed=seed,
-                          outlier_channels=outlier_channels, device=device)
+                          outlier_channels=outlier_channels, device=device, d_k=d_k)
     if tail_fill is not None:
         visible = np.zeros(total_pages * page_block, dtype=bool)
         for b in range(B):
@@ -126,12 +127,12 @@ def make_dense_case(seqlens: Sequence[int], s_q: int = 1, h_q: int = 128,
         hidden = torch.from_numpy(~visible).to(kv.device)
         kv[hidden] = torch.tensor(tail_fill, dtype=dtype, device=kv.device)
     gq = _gen(seed + 10, device)
-    q = torch.randn(B, s_q, h_q, D_K, generator=gq, device=device,
+    q = torch.randn(B, s_q, h_q, d_k, generator=gq, device=device,
                     dtype=torch.float32).to(dtype)
     return DenseCase(q=q, kv_rows=kv, block_table=torch.from_numpy(bt),
                      cache_seqlens=torch.from_numpy(seqlens.astype(np.int32)),
                      page_block=page_block, s_q=s_q, h_q=h_q, causal=causal,
-                     softmax_scale=D_K ** -0.5)
+                     softmax_scale=d_k ** -0.5)
 
 
 @dataclasses.dataclass
@@ -153,7 +154,7 @@ class SparseCase:
 def make_sparse_case(batch: int, s_q: int, topk: int, tokens_per_request: int = 131072,
                      h_q: int = 128, page_block: int = 64, invalid_frac: float = 0.05,
                      seed: int = 0, outlier_channels: int = 0, device="cpu",
-                     with_rows: bool = True) -> SparseCase:
+                     with_rows: bool = True, d_k: int = D_K) -> SparseCase:
     """Token-sparse decode: one contiguous cache of ``tokens_per_request`` rows
     per request (request b owns rows [b*T, (b+1)*T)); each query draws ``topk``
     distinct tokens of its request (seed+3) and exactly round(invalid_frac*topk)
@@ -171,13 +172,13 @@ def make_sparse_case(batch: int, s_q: int, topk: int, tokens_per_request: int = 
     rows = None
     if with_rows:
         rows = make_latent_rows(batch * tokens_per_request, dtype=torch.bfloat16, seed=seed,
-                                outlier_channels=outlier_channels, device=device)
+                                outlier_channels=outlier_channels, device=device, d_k=d_k)
     gq = _gen(seed + 10, device)
-    q = torch.randn(batch, s_q, h_q, D_K, generator=gq, device=device,
+    q = torch.randn(batch, s_q, h_q, d_k, generator=gq, device=device,
                     dtype=torch.float32).to(torch.bfloat16)
     return SparseCase(q=q, kv_rows=rows, indices=torch.from_numpy(idx),
                       tokens_per_request=tokens_per_request, page_block=page_block,
-                      s_q=s_q, h_q=h_q, softmax_scale=D_K ** -0.5)
+                      s_q=s_q, h_q=h_q, softmax_scale=d_k ** -0.5)
 
 
 @dataclasses.dataclass

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for must in ["mla_get_metadata", "mla_decode_with_kvcache", "mla_decode_splitkv", "mla_combine_splits", "mla_quantize_kv_fp8", "mla_read_status",
                  "mla_absorb_q", "mla_up_project", "mla_decode_with_kvcache_noalloc",
                  "mla_metadata_size", "mla_workspace_size", "mla_num_sm_parts", "mla_status_string",
-                 "mla_set_test_stall"]:
+                 "mla_set_test_stall", "mla_quantize_kv_fp8_528", "mla_quantize_kv_fp4_288"]:
         assert must in names
 
 
@@ -88,6 +88,11 @@ def _decode(lib, **kw):
     (dict(scale=float("nan")), 1),
     (dict(batch=0), 1),
     (dict(h_q=64), 2),                                  # not implemented
+    (dict(fp8=4), 1),                                   # no such cache format
+    (dict(fp8=-1), 1),
+    (dict(fp8=2, q_dtype=1), 2),                        # quantised rows pair with bf16 queries
+    (dict(fp8=3, q_dtype=1), 2),
+    (dict(idx=FAKE, topk=64, fp8=0), 2),                # token-sparse decode reads quantised rows
 ])
 def test_decode_argument_checks(lib, kw, code):
     assert _decode(lib, **kw) == code
@@ -100,12 +105,18 @@ def test_metadata_argument_checks(lib):
     assert f(None, 2, 1, 128, 1, 0, 0, 0, 64, 4, FAKE, FAKE, None) == 1        # dense needs lengths
     assert f(None, 2, 1, 128, 1, 64, 1, 1, 64, 4, FAKE, FAKE, None) == 1       # sparse + causal
     assert f(FAKE, 2, 1, 128, 1, 0, 0, 0, 64, 0, FAKE, FAKE, None) == 1        # parts
+    assert f(FAKE, 2, 1, 128, 1, 0, 4, 0, 64, 4, FAKE, FAKE, None) == 1        # no such cache format
+    assert f(FAKE, 2, 1, 16, 1, 0, 2, 0, 64, 4, FAKE, FAKE, None) == 2         # few heads: 16-bit caches
 
 
-def test_quantize_argument_checks(lib):
-    assert lib.mla_quantize_kv_fp8(FAKE, FAKE, -1, None) == 1
-    assert lib.mla_quantize_kv_fp8(ctypes.c_void_p((1 << 20) + 8), FAKE, 4, None) == 1
-    assert lib.mla_quantize_kv_fp8(FAKE, FAKE, 0, None) == 0
+@pytest.mark.parametrize("name", ["mla_quantize_kv_fp8", "mla_quantize_kv_fp8_528", "mla_quantize_kv_fp4_288"])
+def test_quantize_argument_checks(lib, name):
+    f = getattr(lib, name)
+    assert f(FAKE, FAKE, -1, None) == 1
+    assert f(ctypes.c_void_p((1 << 20) + 8), FAKE, 4, None) == 1
+    assert f(FAKE, ctypes.c_void_p((1 << 20) + 8), 4, None) == 1
+    assert f(None, FAKE, 4, None) == 1
+    assert f(FAKE, FAKE, 0, None) == 0
 
 
 @pytest.mark.parametrize("name", ["mla_absorb_q", "mla_up_project"])
