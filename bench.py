@@ -51,6 +51,16 @@ WORKLOADS = {
     "fp8_sparse_b32_sq2_topk32768": dict(kind="sparse", batch=32, s_q=2, topk=32768, causal=False),
     # sparse prefill: 1024 query tokens per request, each with its own top-2048 list
     "fp8_sparse_prefill_b4_sq1024_topk2048": dict(kind="sparse", batch=4, s_q=1024, topk=2048, causal=False),
+    # V4.1 rows of 512 values (d_k = d_v = 512): 528-byte FP8 (e4m3 + UE8M0 per
+    # 32) and 288-byte FP4 (e2m1 + e4m3 per 16), token-sparse and paged
+    "v41_fp8_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False, fmt="fp8_528"),
+    "v41_fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False,
+                                             fmt="fp8_528"),
+    "v41_fp4_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False, fmt="fp4_288"),
+    "v41_fp4_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False,
+                                             fmt="fp4_288"),
+    "v41_fp8_dense_b16_l32768": dict(kind="fp8", batch=16, s_q=1, lens=("fixed", 32768), causal=False, fmt="fp8_528"),
+    "v41_fp4_dense_b16_l32768": dict(kind="fp8", batch=16, s_q=1, lens=("fixed", 32768), causal=False, fmt="fp4_288"),
     # the per-head GEMMs around the kernel (q~ = W^UK^T q^C, o = W^UV o~) for the
     # headline's 64 query tokens x 128 heads; L2 flushed before every step
     "absorb_bf16_t64_h128": dict(kind="absorb", batch=64, s_q=1, h_q=128, causal=False),
@@ -59,6 +69,21 @@ SPARSE_TOKENS = 131072
 DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"
 L2_BYTES = 129e6       # GB300 L2; a workload whose touched bytes per step are below
                        # twice this rotates several index sets between steps
+
+
+# cache row formats: kv_format code, bytes per row, query/key width, library
+# quantiser, oracle dequantiser
+FORMATS = {
+    "bf16": (0, 1152, 576, None, None),
+    "fp16": (0, 1152, 576, None, None),
+    "fp8_656": (1, 656, 576, "mla_quantize_kv_fp8", "dequantize_kv_fp8"),
+    "fp8_528": (2, 528, 512, "mla_quantize_kv_fp8_528", "dequantize_kv_fp8_528"),
+    "fp4_288": (3, 288, 512, "mla_quantize_kv_fp4_288", "dequantize_kv_fp4_288"),
+}
+
+
+def workload_format(w) -> str:
+    return w.get("fmt") or {"dense": "bf16", "few": "fp16"}.get(w["kind"], "fp8_656")
 
 
 def load_peaks():
@@ -130,12 +155,12 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
-def work_counts(seqlens, s_q, causal, h_q=128, row_bytes=1152, indices=None):
+def work_counts(seqlens, s_q, causal, h_q=128, row_bytes=1152, indices=None, d_k=576):
     """Algorithmic FLOPs and bytes of one step (no partials, no expansion):
-    FLOPs = 2 * h_q * (576 + 512) per visible (query, key) pair; bytes = the
-    cache rows read once (1152 B bf16, 656 B fp8; a row shared by the query
-    positions of one request counts once) + q + out + lse + block table or
-    index list."""
+    FLOPs = 2 * h_q * (d_k + 512) per visible (query, key) pair; bytes = the
+    cache rows read once (1152 B bf16, 656 / 528 / 288 B quantised; a row
+    shared by the query positions of one request counts once) + q + out + lse
+    + block table or index list."""
     if indices is not None:
         import numpy as np
         B = indices.shape[0]
@@ -152,8 +177,8 @@ def work_counts(seqlens, s_q, causal, h_q=128, row_bytes=1152, indices=None):
                 pairs += max(0, L - (s_q - 1 - i if causal else 0))
         kv = sum(seqlens) * row_bytes
         meta = sum((L + 63) // 64 for L in seqlens) * 4 + B * 4
-    flops = 2.0 * h_q * (576 + 512) * pairs
-    qb = B * s_q * h_q * 576 * 2
+    flops = 2.0 * h_q * (d_k + 512) * pairs
+    qb = B * s_q * h_q * d_k * 2
     ob = B * s_q * h_q * (512 * 2 + 4)
     return flops, kv + qb + ob + meta, kv
 
@@ -211,9 +236,10 @@ class ClockSampler:
 
 def build_case(w, device):
     import synth
+    d_k = FORMATS[workload_format(w)][2]
     if w["kind"] == "sparse":
         case = synth.make_sparse_case(w["batch"], w["s_q"], w["topk"], tokens_per_request=SPARSE_TOKENS, seed=0,
-                                      outlier_channels=4, device=device)
+                                      outlier_channels=4, device=device, d_k=d_k)
         return case, None
     seqlens = workload_seqlens(w)
     if w["kind"] == "few":
@@ -221,7 +247,7 @@ def build_case(w, device):
                                      causal=w["causal"], seed=0, device=device, shuffle=False)
         return case, seqlens
     case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device,
-                                 outlier_channels=4 if w["kind"] == "fp8" else 0)
+                                 outlier_channels=4 if w["kind"] == "fp8" else 0, d_k=d_k)
     return case, seqlens
 
 
@@ -230,11 +256,12 @@ def torch_dtype(name):
     return getattr(torch, name)
 
 
-def oracle_rate(case, seqlens, budget_s, max_requests=None, raw=None):
+def oracle_rate(case, seqlens, budget_s, max_requests=None, raw=None, dequant="dequantize_kv_fp8"):
     """The float64 oracle on whole requests (all heads, every query position)
-    until the time budget is used. With `raw` (the FP8 rows, on any device)
-    each request's rows are dequantised by the oracle first, inside the timed
-    work. Returns (flops/s, description, requests done, seconds, busy cores)."""
+    until the time budget is used. With `raw` (the quantised rows, on any
+    device) each request's rows are dequantised by the oracle first, inside the
+    timed work. Returns (flops/s, description, requests done, seconds, busy
+    cores)."""
     import oracle
     import synth
     s_q, causal = case.s_q, case.causal
@@ -245,24 +272,24 @@ def oracle_rate(case, seqlens, budget_s, max_requests=None, raw=None):
     for b in range(nreq):
         rows = synth.paged_rows_index(bt[b], seqlens[b], case.page_block)
         if raw is not None:
-            kv = oracle.dequantize_kv_fp8(raw[torch_index(rows, raw.device)].cpu().numpy())
+            kv = getattr(oracle, dequant)(raw[torch_index(rows, raw.device)].cpu().numpy())
         else:
             kv = oracle.to_f64(case.kv_rows[torch_index(rows, case.kv_rows.device)].cpu())
         q = oracle.to_f64(case.q[b].cpu())
         for i in range(s_q):
             L = seqlens[b] - (s_q - 1 - i if causal else 0)
             oracle.attend(q[i], kv[:max(L, 0)], case.softmax_scale)
-            done_flops += 2.0 * case.h_q * 1088 * max(L, 0)
+            done_flops += 2.0 * case.h_q * (q.shape[-1] + 512) * max(L, 0)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt, cpu = time.perf_counter() - t0, time.process_time() - c0
-    what = "dequantised FP8 " if raw is not None else ""
+    what = "dequantised " if raw is not None else ""
     return (done_flops / dt, f"{done} of {len(seqlens)} requests ({what}all {case.h_q} heads, s_q={s_q})", done, dt,
             cpu / dt)
 
 
-def oracle_rate_sparse(q, raw, indices, scale, budget_s):
+def oracle_rate_sparse(q, raw, indices, scale, budget_s, dequant="dequantize_kv_fp8"):
     """The float64 oracle on whole sparse queries: gather the query's rows by
     index, dequantise them, attend; until the time budget is used."""
     import numpy as np
@@ -274,9 +301,9 @@ def oracle_rate_sparse(q, raw, indices, scale, budget_s):
         b, i = n // s_q, n % s_q
         sel = indices[b, i]
         sel = sel[sel >= 0]
-        kv = oracle.dequantize_kv_fp8(raw[torch_index(sel.astype(np.int64), raw.device)].cpu().numpy())
+        kv = getattr(oracle, dequant)(raw[torch_index(sel.astype(np.int64), raw.device)].cpu().numpy())
         oracle.attend(oracle.to_f64(q[b, i].cpu()), kv, scale)
-        done_flops += 2.0 * q.shape[2] * 1088 * len(sel)
+        done_flops += 2.0 * q.shape[2] * (q.shape[-1] + 512) * len(sel)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -305,43 +332,44 @@ def run_ours(args, w, rank, world, device):
     s_q, causal = w["s_q"], w["causal"]
     h_q = w.get("h_q", 128)
     is_fp8 = kind in ("fp8", "sparse")
+    fmt_code, row_bytes, d_k, qname, _ = FORMATS[workload_format(w)]
     q = case.q
     bt = sl = idx = None
     idx_sets = [None]
     if kind == "sparse":
         import synth
-        raw = mla.mla_quantize_kv_fp8(case.kv_rows)          # the FP8 cache, written by the library
+        raw = getattr(mla, qname)(case.kv_rows)              # the quantised cache, written by the library
         case.kv_rows = None
-        kv = raw.view(-1, 64, 1, 656)
+        kv = raw.view(-1, 64, 1, row_bytes)
         # the rows one step touches may fit in L2 (topk 2048: about 50 MB per
         # query position); then several seeded index sets are rotated so that
         # more than twice the L2 passes between two uses of one set
         sets = [case.indices.numpy()]
-        counts = [work_counts(None, s_q, False, row_bytes=656, indices=sets[0])]
+        counts = [work_counts(None, s_q, False, row_bytes=row_bytes, indices=sets[0], d_k=d_k)]
         n_sets = max(1, math.ceil(2 * L2_BYTES / counts[0][2]))
         for k in range(1, n_sets):
             sets.append(synth.make_sparse_case(w["batch"], s_q, w["topk"], tokens_per_request=SPARSE_TOKENS,
                                                seed=1000 + k, with_rows=False).indices.numpy())
-            counts.append(work_counts(None, s_q, False, row_bytes=656, indices=sets[-1]))
+            counts.append(work_counts(None, s_q, False, row_bytes=row_bytes, indices=sets[-1], d_k=d_k))
         flops, algo_bytes, kv_bytes = (statistics.mean(c[j] for c in counts) for j in range(3))
         idx_sets = [torch.from_numpy(x).to(device) for x in sets]
         idx = idx_sets[0]
-        meta_args = dict(batch=q.shape[0], topk=idx.shape[-1], is_fp8=True, device=device)
+        meta_args = dict(batch=q.shape[0], topk=idx.shape[-1], kv_format=fmt_code, device=device)
     else:
         bt = case.block_table.to(device)
         sl = case.cache_seqlens.to(device)
         if kind == "fp8":
-            raw = mla.mla_quantize_kv_fp8(case.kv_rows)
-            kv = raw.view(case.num_blocks, 64, 1, 656)
+            raw = getattr(mla, qname)(case.kv_rows)
+            kv = raw.view(case.num_blocks, 64, 1, row_bytes)
         else:
             kv = case.kvcache_paged()
-        flops, algo_bytes, kv_bytes = work_counts(seqlens, s_q, causal, h_q=h_q, row_bytes=656 if is_fp8 else 1152)
-        meta_args = dict(causal=causal, is_fp8=is_fp8)
+        flops, algo_bytes, kv_bytes = work_counts(seqlens, s_q, causal, h_q=h_q, row_bytes=row_bytes, d_k=d_k)
+        meta_args = dict(causal=causal, kv_format=fmt_code)
     out = torch.empty(q.shape[0], s_q, h_q, 512, dtype=q.dtype, device=device)
     lse = torch.empty(q.shape[0], s_q, h_q, dtype=torch.float32, device=device)
     meta, ns = mla.mla_get_metadata(sl, s_q, h_q, **meta_args)
     stream = torch.cuda.current_stream(device)
-    dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8)
+    dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, kv_format=fmt_code)
 
     def step(k=0):
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
@@ -432,7 +460,7 @@ def run_ours(args, w, rank, world, device):
             idxd = next(it_) if idx is not None else None
             m, n = mla.mla_get_metadata(sld, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
             mla.mla_decode_with_kvcache(dev_in[j][0], kv, btd, sld, 512, m, n, out=outs[j], lse=lses[j],
-                                        softmax_scale=case.softmax_scale, causal=causal, is_fp8=is_fp8,
+                                        softmax_scale=case.softmax_scale, causal=causal, kv_format=fmt_code,
                                         indices=idxd)
             ev_comp[j].record(stream)
             with torch.cuda.stream(s_out):
@@ -606,21 +634,25 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         c = r["case"]
+        dq = FORMATS[workload_format(w)][4] or "dequantize_kv_fp8"
         if w["kind"] == "sparse":
             rate, desc, _, _, busy = oracle_rate_sparse(c.q, r["raw"], c.indices.numpy(), c.softmax_scale,
-                                                        args.cpu_budget)
+                                                        args.cpu_budget, dequant=dq)
         else:
-            rate, desc, _, _, busy = oracle_rate(c, r["seqlens"], args.cpu_budget, raw=r["raw"])
+            rate, desc, _, _, busy = oracle_rate(c, r["seqlens"], args.cpu_budget, raw=r["raw"], dequant=dq)
         cpu = cpu_baseline_line(rate, desc, busy)
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"dense": "bf16", "few": "fp16"}.get(w["kind"], "fp8-e4m3 cache, fp16/bf16 MMA"),
+        "dtype": {"bf16": "bf16", "fp16": "fp16", "fp8_656": "fp8-e4m3 cache, fp16/bf16 MMA",
+                  "fp8_528": "fp8-e4m3 cache (UE8M0 scales), bf16 MMA",
+                  "fp4_288": "fp4-e2m1 cache (e4m3 scales), bf16 MMA"}[workload_format(w)],
         "data": "synthetic",
-        "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": w.get("h_q", 128), "d_qk": 576,
-                   "d_v": 512, "page_block": 64, "causal": w["causal"],
-                   "cache": {"dense": "bf16", "few": "fp16", "fp8": "fp8-656B", "sparse": "fp8-656B"}[w["kind"]],
+        "config": {"workload": args.workload, "batch": w["batch"], "s_q": w["s_q"], "h_q": w.get("h_q", 128),
+                   "d_qk": FORMATS[workload_format(w)][2], "d_v": 512, "page_block": 64, "causal": w["causal"],
+                   "cache": {"bf16": "bf16", "fp16": "fp16", "fp8_656": "fp8-656B", "fp8_528": "fp8-528B",
+                             "fp4_288": "fp4-288B"}[workload_format(w)],
                    "seqlens": (f"topk {w['topk']} of {SPARSE_TOKENS} per request, 5% -1" if w["kind"] == "sparse"
                                else f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
                                else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),
@@ -665,9 +697,10 @@ def run_reference(args, w, rank, world):
         sample = f"float64 oracle, {toks} of {T} tokens x {h} heads per step"
         metric = "absorption GEMMs (q~ = W^UK^T q^C, o = W^UV o~) throughput"
     else:
+        d_k = FORMATS[workload_format(w)][2]
         if w["kind"] == "sparse":
             # one query of one request: its top-k rows gathered
-            sp = synth.make_sparse_case(1, 1, w["topk"], tokens_per_request=SPARSE_TOKENS, seed=0)
+            sp = synth.make_sparse_case(1, 1, w["topk"], tokens_per_request=SPARSE_TOKENS, seed=0, d_k=d_k)
             sel = sp.indices.numpy()[0, 0]
             kv = oracle.to_f64(sp.kv_rows)[sel[sel >= 0]]
             q = oracle.to_f64(sp.q[0])
@@ -675,7 +708,7 @@ def run_reference(args, w, rank, world):
         else:
             seqlens = workload_seqlens(w)
             case = synth.make_dense_case(seqlens[:1], s_q=w["s_q"], h_q=w.get("h_q", 128), causal=w["causal"],
-                                         seed=0)
+                                         seed=0, d_k=d_k)
             rows = synth.paged_rows_index(case.block_table.numpy()[0], seqlens[0], 64)
             kv = oracle.to_f64(case.kv_rows)[rows]
             q = oracle.to_f64(case.q[0])
@@ -686,7 +719,7 @@ def run_reference(args, w, rank, world):
         t_full = time.perf_counter() - t0
         heads = int(max(1, min(hq, hq * budget / max(t_full, 1e-6))))
         run = lambda: oracle.attend(q[0, :heads], kv, scale)
-        flops = 2.0 * heads * 1088 * L
+        flops = 2.0 * heads * (d_k + 512) * L
         sample = f"float64 oracle, one request of {L} tokens x {heads} heads per step (s_q position 0)"
     for _ in range(args.warmup):
         run()
