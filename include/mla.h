@@ -169,9 +169,11 @@ MLA_API size_t mla_workspace_size(int batch, int s_q, int h_q, int num_sm_parts)
  * instead. Out of range -- a query entry beyond 65504 in magnitude (saturated
  * to +-65504) or a block scale above 146 (block amax above 65408) -- the
  * status word records MLA_ERR_RANGE.
- * The V4.1 rows run in bf16: e4m3 x 2^k and e2m1 x e4m3 are exact in bf16
- * while the UE8M0 scale is at most 2^15 (byte 142; beyond it MLA_ERR_RANGE)
- * and the value is at least 2^-126 (smaller ones may lose bits).
+ * The V4.1 rows run in fp16 as well (query rounded to fp16, with the same
+ * 65504 limit): e2m1 x e4m3 is always exact in fp16; e4m3 x 2^k is exact for
+ * k in [-15, 7]; a block with a smaller scale (amax below 448 * 2^-16) carries
+ * an absolute error of at most 2^-25, and a larger one (amax above 57344,
+ * UE8M0 byte above 134) is reported as MLA_ERR_RANGE.
  * Every cache type splits the dims of a score between the two CTAs of a
  * pair, which exchange fp16 factors 2^(partial score - partial max). The
  * result is certified exact (to fp16 precision) for a row of a 64-token tile

@@ -121,20 +121,29 @@ constexpr uint32_t kEBar = 1;                           // named barrier of the 
 // V4.1 FP4 rows (288 B): e2m1 [0,256) (value 2i in the low nibble of byte i),
 // 32 e4m3 scales [256,288)
 
+#ifndef V41_FP4_NS
+#define V41_FP4_NS 3
+#endif
+#ifndef V41_FP8_NS
+#define V41_FP8_NS 3
+#endif
 // per-mode layout (offsets from a 1024-B aligned base) and barrier indices
 template <int kMode>
 struct Cfg {
   static constexpr bool kFp16 = kMode == MODE_FP16;
   static constexpr bool kQuant = kMode >= MODE_FP8;        // quantised rows: dequant warps
-  static constexpr bool kF656 = kMode == MODE_FP8 || kMode == MODE_FP8_SPARSE;
   static constexpr bool kV41 = kMode >= MODE_V41_FP8;      // 512-value rows, no separate RoPE part
   static constexpr bool kFp4 = kMode >= MODE_V41_FP4;
   static constexpr bool kSparse = kMode == MODE_FP8_SPARSE || kMode == MODE_V41_FP8_SPARSE ||
                                   kMode == MODE_V41_FP4_SPARSE;
-  // 16-bit operand type of the latent QK^T and P . V: bf16, except fp16 for
-  // fp16 caches and for 656-byte FP8 rows (whose products are formed in fp16)
-  static constexpr bool kLatBf16 = !(kFp16 || kF656);
-  static constexpr int kNS = kQuant ? 3 : 5;              // KV ring slots (tiles)
+  // 16-bit operand type of the latent QK^T and P . V: bf16 for bf16 caches;
+  // fp16 for fp16 caches and for every quantised row, whose products are
+  // formed in fp16 (cheaper to form than bf16, and exact in the ranges below)
+  static constexpr bool kLatBf16 = !(kFp16 || kQuant);
+  // operand slot: four 64-wide chunks and, unless the row is a V4.1 row, a
+  // 32-wide RoPE chunk
+  static constexpr uint32_t kSlotBytes = kV41 ? 4 * kKChunk : kSlot;
+  static constexpr int kNS = kQuant ? (kFp4 ? V41_FP4_NS : (kV41 ? V41_FP8_NS : 3)) : 5;  // KV ring slots (tiles)
   // quantised rows: two more dequant warps (12, 13) and the P . V issuer (14)
   static constexpr int kThreads = kQuant ? 480 : 384;
   static constexpr int kPvWarp = kQuant ? 14 : 2;         // its lane 0 issues P . V
@@ -150,8 +159,8 @@ struct Cfg {
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
   static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
   static constexpr uint32_t OFF_QR = OFF_XS + kXStride;  // 32 RoPE dims of Q: 128 rows x 64 B
-  static constexpr uint32_t OFF_RING = OFF_QR + 128 * 64;
-  static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlot;
+  static constexpr uint32_t OFF_RING = OFF_QR + (kV41 ? 0 : 128 * 64);
+  static constexpr uint32_t OFF_RAW = OFF_RING + kNS * kSlotBytes;
   static constexpr uint32_t OFF_BAR = OFF_RAW + (kQuant ? kRawNS * kRawSlot : 0);
   static constexpr uint32_t B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1,
                             B_SFULL = B_QEMPTY + 1, B_SEMPTY = B_SFULL + 1, B_PFULL = B_SEMPTY + 1,
@@ -165,7 +174,11 @@ struct Cfg {
 };
 static_assert(Cfg<MODE_BF16>::kSmemBytes <= 232448, "shared memory");
 static_assert(Cfg<MODE_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_FP8>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_V41_FP8>::kSmemBytes <= 232448, "shared memory");
 static_assert(Cfg<MODE_V41_FP8_SPARSE>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_V41_FP4>::kSmemBytes <= 232448, "shared memory");
+static_assert(Cfg<MODE_V41_FP4_SPARSE>::kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ bool warp_ok(bool x) { return __all_sync(0xffffffffu, x); }
 
@@ -194,10 +207,11 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint16_t v) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
+// 2^k as an fp16 pair: normal for k in [-14, 15], subnormal down to 2^-24,
+// zero below (k above 15 does not occur: such blocks are reported)
+__device__ __forceinline__ uint32_t f16x2_pow2(int k) {
+  const uint32_t h = k >= -14 ? (uint32_t)(k + 15) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
+  return h | (h << 16);
 }
 // four bytes of e2m1 pairs -> four f16 pairs (exact); byte i gives h[i], its
 // low nibble in the low half
@@ -211,13 +225,7 @@ __device__ __forceinline__ void cvt_e2m1x4_f16x2(uint32_t w, uint32_t* h) {
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
       : "r"(w));
 }
-// an f16 pair whose values are normal (or zero) with at most 7 significant
-// bits -> the bf16 pair of the same values times 2^-112: the 5-bit exponent
-// field moves into the low bits of bf16's 8-bit field (bias 15 read as bias
-// 127) and the mantissa loses only zero bits
-__device__ __forceinline__ uint32_t f16x2_as_bf16x2_m112(uint32_t h) {
-  return ((h & 0x7FFF7FFFu) >> 3) | (h & 0x80008000u);
-}
+
 
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads, 1)
@@ -225,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
                       const __grid_constant__ CUtensorMap tm_kvr, const __grid_constant__ CUtensorMap tm_sc,
                       const DecodeParams p) {
   using C = Cfg<kMode>;
-  constexpr bool kFp16 = C::kFp16, kQuant = C::kQuant, kF656 = C::kF656, kV41 = C::kV41, kFp4 = C::kFp4,
+  constexpr bool kFp16 = C::kFp16, kQuant = C::kQuant, kV41 = C::kV41, kFp4 = C::kFp4,
                  kSparse = C::kSparse;
   constexpr int NS = C::kNS;
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
@@ -380,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             if constexpr (kV41) continue;  // the dequant warps fill the whole operand slot
           }
           if (!wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard)) { stop = true; break; }
-          const uint32_t slot = sb + C::OFF_RING + s * kSlot;
+          const uint32_t slot = sb + C::OFF_RING + s * C::kSlotBytes;
           if constexpr (kQuant) {
             // the RoPE dims are bf16 in the row: straight into the operand slot
             mbar_arrive_expect_tx(bar(C::B_FULL + s), kRChunk);
@@ -428,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           if (lane == 0) mbar_arrive_expect_tx(bar(C::B_FULL + s), 64u * 64u);
           __syncwarp();
           if (lane < 16)
-            tma_gather4(sb + C::OFF_RING + s * kSlot + 4 * kKChunk + lane * 4 * 64, &tm_kvr, bar(C::B_FULL + s),
+            tma_gather4(sb + C::OFF_RING + s * C::kSlotBytes + 4 * kKChunk + lane * 4 * 64, &tm_kvr, bar(C::B_FULL + s),
                         528 + 64 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
           last_g[s] = g;
         }
@@ -452,11 +460,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       }
     }
   } else if (kQuant && ok && (warp == 2 || warp == 3 || warp == 12 || warp == 13)) {
-    // ---------------- dequant: codes x block scale -> 16-bit operand tiles ----------------
-    // 656-byte rows: e4m3 x fp32 scale -> fp16 (fp16 keeps 11 bits of the
-    // product; their latent QK^T and P . V run as fp16 x fp16, the RoPE QK^T
-    // stays bf16 x bf16). V4.1 rows: e4m3 x 2^k and e2m1 x e4m3 are exact in
-    // bf16 and run as bf16 x bf16.
+    // ---------------- dequant: codes x block scale -> fp16 operand tiles ----------------
+    // (fp16 keeps 11 bits of the product; the latent QK^T and P . V of
+    // quantised rows run as fp16 x fp16, the RoPE QK^T of 656-byte rows stays
+    // bf16 x bf16). 656: e4m3 x fp32 scale, rounded through the fp16 copy of
+    // the scale. 528: e4m3 x 2^k, exact for k in [-15, 7]. 288: e2m1 x e4m3,
+    // always exact (magnitudes in [2^-10, 2688]).
     const int tid = (warp < 4 ? warp - 2 : warp - 10) * 32 + lane;  // 0..127 over the four warps
     PieceIter it(p, part);
     Piece pc;
@@ -466,8 +475,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     // 65408) keeps its fp16 copy at most 146 (an fp16 value), so no product
     // code x scale (|code| <= 448) exceeds fp16's 65504
     float sc_max = 0.f;
-    // 528: largest UE8M0 byte seen: up to 142 (k <= 15, block amax <= 448 *
-    // 2^15) the factor 2^(k+112) below is a bf16 value
+    // 528: largest UE8M0 byte seen: up to 134 (k <= 7, block amax <= 448 * 2^7)
+    // no product code x 2^k exceeds fp16's 65504
     uint32_t ue_max = 0u;
     while (!failed && it.next(pc)) {
       MaskStream<kSparse> ms;
@@ -481,64 +490,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           break;
         }
         const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
-        const uint32_t slot = sb + C::OFF_RING + s * kSlot;
-        const uint8_t* scales = smem + C::OFF_RAW + rs * C::kRawSlot + C::kRawLat;
-        // 64 rows x 32 units of 8 values; consecutive lanes take consecutive
-        // units of one row (conflict-free loads, 16-B swizzled stores)
-#pragma unroll 4
-        for (int it2 = 0; it2 < 16; ++it2) {
-          const int id = it2 * 128 + tid;
-          const int row = id >> 5, unit = id & 31;
-          uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-          if ((vmask >> row) & 1ull) {
-            // the row's 16 scale bytes: dense 16 B per row; sparse: rows
-            // 4k..4k+3 share a 128-B unit
-            const uint8_t* sc_row = scales + (kSparse ? (row >> 2) * 128 + (row & 3) * 16 : row * 16);
-            if constexpr (kFp4) {
-              // 8 e2m1 values (4 bytes) x this CTA's e4m3 scale of their 16:
-              // e2m1 -> f16 is exact, moved to bf16 x 2^-112 by a shift,
-              // times bf16(scale x 2^112): exact (at most 5 significant bits,
-              // magnitudes in [2^-10, 2688])
-              const uint32_t wd = ld_shared_u32(raw + row * 128 + unit * 4);
-              const uint32_t sc = sc_row[unit >> 1];
-              const float sv = __half2float(__ushort_as_half((uint16_t)(cvt_e4m3x2_f16x2((uint16_t)sc) & 0xFFFFu)));
-              const uint32_t sbf = __float_as_uint(sv * 0x1p112f) >> 16;
-              const uint32_t s2 = sbf | (sbf << 16);
-              uint32_t h[4];
-              cvt_e2m1x4_f16x2(wd, h);
-              w0 = mul_bf16x2(f16x2_as_bf16x2_m112(h[0]), s2);
-              w1 = mul_bf16x2(f16x2_as_bf16x2_m112(h[1]), s2);
-              w2 = mul_bf16x2(f16x2_as_bf16x2_m112(h[2]), s2);
-              w3 = mul_bf16x2(f16x2_as_bf16x2_m112(h[3]), s2);
-            } else {
-              uint32_t lo, hi;
-              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 256 + unit * 8));
-              if constexpr (kV41) {
-                // 8 e4m3 x 2^k (UE8M0 byte k + 127 of their 32 values): e4m3 ->
-                // f16 is exact, moved to bf16 x 2^-112 by a shift, times
-                // 2^(k+112) (exact while k <= 15)
-                const uint32_t ue = sc_row[8 * rank + (unit >> 2)];
-                ue_max = ue > ue_max ? ue : ue_max;
-                const uint32_t f = (ue + 112u) << 7;
-                const uint32_t f2 = f | (f << 16);
-                w0 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF))), f2);
-                w1 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16))), f2);
-                w2 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF))), f2);
-                w3 = mul_bf16x2(f16x2_as_bf16x2_m112(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16))), f2);
-              } else {
-                const float sc = reinterpret_cast<const float*>(sc_row)[2 * rank + (unit >> 4)];
-                sc_max = fmaxf(sc_max, sc);
-                // e4m3 -> f16 is exact; the product rounds once more through the
-                // fp16 copy of the scale (both roundings are below 2^-11 relative)
-                const uint32_t sc2 = pack_f16x2(sc, sc);
-                w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo & 0xFFFF)), sc2);
-                w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(lo >> 16)), sc2);
-                w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi & 0xFFFF)), sc2);
-                w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(hi >> 16)), sc2);
-              }
-            }
+        const uint32_t slot = sb + C::OFF_RING + s * C::kSlotBytes;
+        const uint32_t scales = raw + C::kRawLat;
+        // The thread converts unit `lane` (8 values) of rows wq, wq + 4, ...,
+        // wq + 60; consecutive lanes take consecutive units of one row
+        // (conflict-free loads, 16-B swizzled stores). All 16 rows' codes and
+        // scales are loaded first and converted after: the shared-memory
+        // accesses are ordered asm, so interleaving them row by row would
+        // serialise every row's load -> convert -> store chain.
+        const int wq = tid >> 5;
+        uint32_t r0[16], r1[16], sc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int row = 4 * k + wq;
+          // the row's 16 scale bytes: dense 16 B per row; sparse: rows
+          // 4k..4k+3 share a 128-B unit
+          const uint32_t sc_row = scales + (kSparse ? (row >> 2) * 128 + (row & 3) * 16 : row * 16);
+          if constexpr (kFp4) {
+            r0[k] = ld_shared_u32(raw + row * 128 + lane * 4);
+            sc[k] = ld_shared_u8(sc_row + (lane >> 1));
+          } else {
+            ld_shared_v2(raw + row * 256 + lane * 8, r0[k], r1[k]);
+            sc[k] = kV41 ? ld_shared_u8(sc_row + 8 * rank + (lane >> 2))
+                         : ld_shared_u32(sc_row + 4 * (2 * rank + (lane >> 4)));
           }
-          st_shared_v4(slot + (unit >> 3) * kKChunk + row * 128 + (((unit & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int row = 4 * k + wq;
+          const bool live = (vmask >> row) & 1ull;
+          uint32_t w0, w1, w2, w3;
+          if constexpr (kFp4) {
+            // 8 e2m1 values (4 bytes) x this CTA's e4m3 scale of their 16:
+            // both -> f16 exactly, and the product (at most 5 significant
+            // bits, magnitude in [2^-10, 2688]) is exact in fp16
+            const uint32_t s2 = cvt_e4m3x2_f16x2((uint16_t)(sc[k] | (sc[k] << 8)));
+            uint32_t h[4];
+            cvt_e2m1x4_f16x2(r0[k], h);
+            w0 = mul_f16x2(h[0], s2);
+            w1 = mul_f16x2(h[1], s2);
+            w2 = mul_f16x2(h[2], s2);
+            w3 = mul_f16x2(h[3], s2);
+          } else if constexpr (kV41) {
+            // 8 e4m3 x 2^k (UE8M0 byte k + 127 of their 32 values): e4m3 ->
+            // f16 is exact, and so is the product for k in [-15, 7]; below
+            // that it rounds to fp16's subnormal grid (absolute error at most
+            // 2^-25)
+            const uint32_t ue = sc[k];
+            if (live) ue_max = ue > ue_max ? ue : ue_max;
+            const uint32_t f2 = f16x2_pow2((int)ue - 127);
+            w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r0[k] & 0xFFFF)), f2);
+            w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r0[k] >> 16)), f2);
+            w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r1[k] & 0xFFFF)), f2);
+            w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r1[k] >> 16)), f2);
+          } else {
+            const float scf = __uint_as_float(sc[k]);
+            if (live) sc_max = fmaxf(sc_max, scf);
+            // e4m3 -> f16 is exact; the product rounds once more through the
+            // fp16 copy of the scale (both roundings are below 2^-11 relative)
+            const uint32_t sc2 = pack_f16x2(scf, scf);
+            w0 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r0[k] & 0xFFFF)), sc2);
+            w1 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r0[k] >> 16)), sc2);
+            w2 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r1[k] & 0xFFFF)), sc2);
+            w3 = mul_f16x2(cvt_e4m3x2_f16x2((uint16_t)(r1[k] >> 16)), sc2);
+          }
+          if (!live) w0 = w1 = w2 = w3 = 0u;  // masked rows: zero values, whatever the bytes
+          st_shared_v4(slot + (lane >> 3) * kKChunk + row * 128 + (((lane & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -548,7 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
       }
     }
-    if (__any_sync(0xffffffffu, !(sc_max <= 146.0f) || ue_max > 142u) && lane == 0) atomicOr(p.status, STATUS_RANGE);
+    if (__any_sync(0xffffffffu, !(sc_max <= 146.0f) || ue_max > 134u) && lane == 0) atomicOr(p.status, STATUS_RANGE);
   } else if (ok && lane == 0 && (warp == 1 || warp == C::kPvWarp)) {
     // ---------------- UMMA issue ----------------
     // 16-bit operand type of the latent QK^T / P.V (fp16 for fp16 and FP8
@@ -564,7 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     auto issue_qk = [&](int g) {
       const int s = g % NS;
       const uint32_t dS = tmem + kColS;
-      const uint32_t slot = sb + C::OFF_RING + s * kSlot;
+      const uint32_t slot = sb + C::OFF_RING + s * C::kSlotBytes;
       const uint64_t d_k = sdesc_sw128(slot, 16, 1024);
       const uint64_t d_kr = sdesc_sw64(slot + 4 * kKChunk, 16, 512);
 #pragma unroll
@@ -582,7 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
     };
     // O[:, this CTA's 256 dims] (+)= P V of tile g; frees P and the ring slot
     auto issue_pv = [&](int g, bool first) {
-      const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (g % NS) * kSlot, kKChunk, 1024);
+      const uint64_t d_v = sdesc_sw128(sb + C::OFF_RING + (g % NS) * C::kSlotBytes, kKChunk, 1024);
       const uint32_t tp = tmem + kColP + 32u * (uint32_t)(g & 1);  // P as the A operand, from TMEM
       umma_ts(tmem, tp, d_v, idesc_pv, first ? 0u : 1u);
       umma_ts(tmem, tp + 8u, d_v + 128, idesc_pv, 1u);
@@ -670,7 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           const uint4 x = __ldg(src + 16 * half + k);
           r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
         }
-        if constexpr (kF656) {  // latent operands of 656-byte FP8 rows are fp16
+        if constexpr (kQuant) {  // latent operands of quantised rows are fp16
           float qmax = 0.f;
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
@@ -900,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         if (!kQuant && vm != ~0ull) {
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
           // turn into NaN inside P . V (the dequant warps do this for FP8 rows)
-          const uint32_t slot = sb + C::OFF_RING + (g % NS) * kSlot;
+          const uint32_t slot = sb + C::OFF_RING + (g % NS) * C::kSlotBytes;
           for (int e2 = pid; e2 < 64 * 32; e2 += 128) {
             const int row = e2 >> 5, u = e2 & 31;
             if (!((vm >> row) & 1ull))

@@ -12,8 +12,8 @@ row, and so is its value.
 * Gathering is exact: with one key per query dominating by about 196 log2
   units (the others' weights underflow fp32), the output is that key's
   dequantised row bit for bit.
-* A UE8M0 scale beyond 2^15 and halves of a score more than about 22 binades
-  apart are reported as MLA_ERR_RANGE.
+* A UE8M0 scale beyond 2^7, a query entry beyond fp16's range and halves of
+  a score more than about 22 binades apart are reported as MLA_ERR_RANGE.
 """
 import numpy as np
 import pytest
@@ -265,10 +265,11 @@ def test_paged_gather_exact(name):
 
 
 def test_fp8_528_scale_beyond_range_is_reported():
-    """A block amax of 3e7 needs 2^16 > 2^15: reported, not passed silently;
-    2^15 (amax 1e7) still decodes within tolerance."""
+    """The 528-byte rows are dequantised to fp16: a block amax of 6e4 needs a
+    scale of 2^8, whose largest products exceed 65504: reported, not passed
+    silently; 2^7 (amax 5e4) still decodes within tolerance."""
     f = FORMATS["fp8_528"]
-    for amax, ok in [(1e7, True), (3e7, False)]:
+    for amax, ok in [(5e4, True), (6e4, False)]:
         case = synth.make_dense_case([100], seed=98, d_k=512)
         case.kv_rows[3, 40] = amax
         case.q[..., 40] = 0          # keep the scores ordinary
@@ -279,6 +280,17 @@ def test_fp8_528_scale_beyond_range_is_reported():
             assert_close_attn(out, lse, ro, rl, "528 scale 2^15")
         else:
             assert st == MLA_ERR_RANGE and bits & 8, (st, bits)
+
+
+@pytest.mark.parametrize("name", list(FORMATS))
+def test_query_beyond_fp16_is_reported(name):
+    """The latent product of quantised rows runs in fp16: a bf16 query entry
+    beyond 65504 is saturated and reported."""
+    f = FORMATS[name]
+    case = synth.make_dense_case([100, 7], seed=100, d_k=512)
+    case.q[1, 0, 5, 300] = 1e5
+    _, _, _, (st, bits) = _run_dense(case, f)
+    assert st == MLA_ERR_RANGE and bits & 8, (st, bits)
 
 
 @pytest.mark.parametrize("name", list(FORMATS))
