@@ -155,7 +155,12 @@ struct Cfg {
   // 288: this CTA's 16 e4m3 scales); the sparse gather writes them four rows
   // (64 B) at a time into 128-B aligned units
   static constexpr uint32_t kRawSc = kSparse ? 16 * 128 : 64 * 16;
-  static constexpr uint32_t kRawSlot = kRawLat + kRawSc;
+  // 656-byte rows: this CTA's 32 RoPE dims (bf16) of the 64 rows, 64-byte
+  // swizzled like the operand slot's RoPE chunk (both 512-B aligned), copied
+  // there by the dequant warps; so the producer never waits for a free operand
+  // slot and its raw loads run kRawNS tiles ahead
+  static constexpr uint32_t kRawRope = kV41 ? 0 : kRChunk;
+  static constexpr uint32_t kRawSlot = kRawLat + kRawSc + kRawRope;
   static constexpr uint32_t OFF_XR = 0;                  // peer's message
   static constexpr uint32_t OFF_XS = OFF_XR + kXStride;  // own message, staged for the copy
   static constexpr uint32_t OFF_QR = OFF_XS + kXStride;  // 32 RoPE dims of Q: 128 rows x 64 B
@@ -256,9 +261,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      // producer (RoPE part) and the dequant warps of quantised rows; V4.1
-      // rows have no separate RoPE part, so only the dequant warps fill a slot
-      mbar_init(bar(C::B_FULL + s), kV41 ? kDequantWarps : (kQuant ? 1 + kDequantWarps : 1));
+      // the producer's copy (16-bit caches) or the dequant warps (quantised rows)
+      mbar_init(bar(C::B_FULL + s), kQuant ? kDequantWarps : 1);
       mbar_init(bar(C::B_EMPTY + s), 1);
     }
     mbar_init(bar(C::B_QFULL), kEWarps + 1);  // E warps (latent into TMEM) + producer (RoPE TMA)
@@ -381,23 +385,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             const int rs = g % C::kRawNS;
             if (!wait(bar(C::B_REMPTY + rs), ((g / C::kRawNS) & 1) ^ 1, guard)) { stop = true; break; }
             const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
-            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), C::kRawLat + C::kRawSc);
+            mbar_arrive_expect_tx(bar(C::B_RFULL + rs), C::kRawSlot);
             tma_load_2d(raw, &tm_kv, bar(C::B_RFULL + rs), (int)C::kRawRow * (int)rank, page * kTile, pol_kv);
             tma_load_2d(raw + C::kRawLat, &tm_sc, bar(C::B_RFULL + rs), kScX, page * kTile, pol_kv);
+            if constexpr (!kV41)  // the RoPE dims are bf16 in the row
+              tma_load_2d(raw + C::kRawLat + C::kRawSc, &tm_kvr, bar(C::B_RFULL + rs), 528 + 64 * (int)rank,
+                          page * kTile, pol_kv);
             last_rg[rs] = g;
-            if constexpr (kV41) continue;  // the dequant warps fill the whole operand slot
+            continue;  // the dequant warps fill the operand slot
           }
           if (!wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard)) { stop = true; break; }
           const uint32_t slot = sb + C::OFF_RING + s * C::kSlotBytes;
-          if constexpr (kQuant) {
-            // the RoPE dims are bf16 in the row: straight into the operand slot
-            mbar_arrive_expect_tx(bar(C::B_FULL + s), kRChunk);
-            tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), 528 + 64 * (int)rank, page * kTile, pol_kv);
-          } else {
-            mbar_arrive_expect_tx(bar(C::B_FULL + s), kSlot);
-            tma_load_3d(slot, &tm_kv, bar(C::B_FULL + s), 0, page * kTile, 4 * (int)rank, pol_kv);
-            tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), xr, page * kTile, pol_kv);
-          }
+          mbar_arrive_expect_tx(bar(C::B_FULL + s), kSlot);
+          tma_load_3d(slot, &tm_kv, bar(C::B_FULL + s), 0, page * kTile, 4 * (int)rank, pol_kv);
+          tma_load_2d(slot + 4 * kKChunk, &tm_kvr, bar(C::B_FULL + s), xr, page * kTile, pol_kv);
           last_g[s] = g;
         } else {
           // sparse: TMA gather4, four rows per copy; lane j < 16 fetches rows
@@ -419,26 +420,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             const int c = __shfl_sync(0xffffffffu, s1, row & 31);
             r[q] = row < 32 ? a : c;
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (C::kRawRow + 16));
+          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_RFULL + rs), 64u * (C::kRawRow + 16) + C::kRawRope);
           __syncwarp();
           if (lane < 16) {
             const uint32_t fb = bar(C::B_RFULL + rs);
             tma_gather4(raw + lane * 4 * C::kRawRow, &tm_kv, fb, (int)C::kRawRow * (int)rank, r[0], r[1], r[2], r[3],
                         pol_kv);
             tma_gather4(raw + C::kRawLat + lane * 128, &tm_sc, fb, kScX, r[0], r[1], r[2], r[3], pol_kv);
+            // 656-byte rows: the RoPE dims (bf16), 64-byte swizzled by the copy
+            if constexpr (!kV41)
+              tma_gather4(raw + C::kRawLat + C::kRawSc + lane * 4 * 64, &tm_kvr, fb, 528 + 64 * (int)rank, r[0], r[1],
+                          r[2], r[3], pol_kv);
           }
           last_rg[rs] = g;
-          if constexpr (kV41) continue;
-          // the RoPE dims (bf16 in the row) go straight into the operand slot,
-          // four rows per copy, 64-byte swizzled by the copy; the dequant
-          // warps fill the latent part
-          if (!warp_ok(wait(bar(C::B_EMPTY + s), ((g / NS) & 1) ^ 1, guard))) { stop = true; break; }
-          if (lane == 0) mbar_arrive_expect_tx(bar(C::B_FULL + s), 64u * 64u);
-          __syncwarp();
-          if (lane < 16)
-            tma_gather4(sb + C::OFF_RING + s * C::kSlotBytes + 4 * kKChunk + lane * 4 * 64, &tm_kvr, bar(C::B_FULL + s),
-                        528 + 64 * (int)rank, r[0], r[1], r[2], r[3], pol_kv);
-          last_g[s] = g;
         }
       }
     }
@@ -556,6 +550,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           }
           if (!live) w0 = w1 = w2 = w3 = 0u;  // masked rows: zero values, whatever the bytes
           st_shared_v4(slot + (lane >> 3) * kKChunk + row * 128 + (((lane & 7) ^ (row & 7)) << 4), w0, w1, w2, w3);
+        }
+        if constexpr (C::kRawRope > 0) {
+          // the RoPE chunk, already in the operand layout (masked tokens'
+          // scores are -inf, and RoPE dims are not part of the value)
+#pragma unroll
+          for (int i = 0; i < (int)(C::kRawRope / 16 / 128); ++i) {
+            const uint32_t off = (uint32_t)(i * 128 + tid) * 16u;
+            const float4 v = ld_shared_v4f(raw + C::kRawLat + C::kRawSc + off);
+            st_shared_v4(slot + 4 * kKChunk + off, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                         __float_as_uint(v.w));
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
