@@ -369,11 +369,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
       if (stop) break;
       ++qn;
       int pg_next = 0;               // dense: page of tile t, loaded one tile ahead
-      int n0 = 0, n1 = 0;            // sparse: indices of tile t, loaded ahead
+      // sparse: indices of tiles t, t+1, t+2, loaded three tiles ahead, so that
+      // the gathers of tile t find its indices in registers
+      int n0 = 0, n1 = 0, m0 = 0, m1 = 0, k0 = 0, k1 = 0;
       if constexpr (!kSparse) {
         pg_next = raw_page(b, pc.t0);
       } else {
         sparse_fetch(p, pc.v, pc.t0, n0, n1);
+        sparse_fetch(p, pc.v, pc.t0 + 1, m0, m1);
+        sparse_fetch(p, pc.v, pc.t0 + 2, k0, k1);
       }
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         const int s = g % NS;
@@ -407,7 +411,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           // that is -1 or out of range is fetched as row 0 and masked later.
           const int rs = g % C::kRawNS;
           const int idx[2] = {n0, n1};
-          if (t + 1 < pc.t1) sparse_fetch(p, pc.v, t + 1, n0, n1);  // consumed next tile
+          n0 = m0;
+          n1 = m1;
+          m0 = k0;
+          m1 = k1;
+          if (t + 3 < pc.t1) sparse_fetch(p, pc.v, t + 3, k0, k1);  // consumed three tiles on
           if (!warp_ok(wait(bar(C::B_REMPTY + rs), ((g / C::kRawNS) & 1) ^ 1, guard))) { stop = true; break; }
           const uint32_t raw = sb + C::OFF_RAW + rs * C::kRawSlot;
           const int s0 = (idx[0] >= 0 && (int64_t)idx[0] < p.num_rows) ? idx[0] : 0;
@@ -568,6 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           mbar_arrive(bar(C::B_FULL + s));
           mbar_arrive(bar(C::B_REMPTY + rs));
         }
+        ms.prefetch(p, t);
       }
     }
     if (__any_sync(0xffffffffu, !(sc_max <= 146.0f) || ue_max > 134u) && lane == 0) atomicOr(p.status, STATUS_RANGE);
@@ -773,6 +782,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
           bulk_copy_to_peer(xr_remote, xs, kXBytes, xfull_remote);
           mbar_arrive(bar(C::B_XSFULL));
         }
+        ms.prefetch(p, t);
       }
     }
   } else if (ok && warp >= 8 && warp < 12) {

@@ -337,27 +337,38 @@ template <bool kSparse>
 struct MaskStream {
   int v, len;
   PageWindow w;
-  int a0, a1, c0, c1;  // sparse: indices of the next two tiles
+  // sparse: indices of tiles t, t+1, t+2 (each lane holds entries lane and
+  // lane + 32 of a tile). Tile t+3 is fetched by prefetch(), which the caller
+  // issues after its work on tile t, so that no index load is outstanding
+  // while that work runs.
+  int a0, a1, c0, c1, e0, e1;
   __device__ __forceinline__ void start(const DecodeParams& p, const Piece& pc) {
     v = pc.v;
     len = pc.len;
     if constexpr (kSparse) {
       sparse_fetch(p, v, pc.t0, a0, a1);
       sparse_fetch(p, v, pc.t0 + 1, c0, c1);
+      sparse_fetch(p, v, pc.t0 + 2, e0, e1);
     } else {
       w.start(p, v % p.batch, pc.t0);
     }
   }
   __device__ __forceinline__ uint64_t next(const DecodeParams& p, int t, bool report) {
     if constexpr (kSparse) {
-      const uint64_t m = sparse_mask(p, a0, a1, report);
-      a0 = c0;
-      a1 = c1;
-      sparse_fetch(p, v, t + 2, c0, c1);
-      return m;
+      return sparse_mask(p, a0, a1, report);
     } else {
       w.advance(p, t);
       return dense_mask(p, w.get(t), t, len, report);
+    }
+  }
+  // after the work on tile t: shift the ring and fetch tile t+3
+  __device__ __forceinline__ void prefetch(const DecodeParams& p, int t) {
+    if constexpr (kSparse) {
+      a0 = c0;
+      a1 = c1;
+      c0 = e0;
+      c1 = e1;
+      sparse_fetch(p, v, t + 3, e0, e1);
     }
   }
 };
