@@ -980,7 +980,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
               *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(w[k], w[k + 1], w[k + 2], w[k + 3]);
           }
         } else {
-          float* dst = p.o_part + ((int64_t)pc.split * 128 + h) * kDV + 256 * rank + 32 * cc;
+          const int d0 = 256 * (int)rank + 32 * cc;
 #pragma unroll
           for (int k = 0; k < 32; k += 2) {
             const float2 ac = f2_unpack(f2_mul(f2_pack(__uint_as_float(r[k]), __uint_as_float(r[k + 1])), inv2));
@@ -988,7 +988,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
             r[k + 1] = __float_as_uint(ac.y);
           }
 #pragma unroll
-          for (int k = 0; k < 32; k += 8) st_global_v8(dst + k, r + k);
+          for (int k = 0; k < 32; k += 8) st_global_v8(p.o_part + opart_index(pc.split, 128, h, d0 + k), r + k);
         }
       };
       uint32_t ra[32], rb[32];

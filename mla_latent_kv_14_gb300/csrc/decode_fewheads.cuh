@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int h = 0; h < kNH; ++h)
-            p.o_part[((int64_t)pc.split * kNH + h) * kDV + d] = __uint_as_float(o[h]) * inv[h];
+            p.o_part[opart_index(pc.split, kNH, h, d)] = __uint_as_float(o[h]) * inv[h];
         }
       }
       if (warp == 2 && lane < kNH) {

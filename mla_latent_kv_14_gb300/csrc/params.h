@@ -38,12 +38,18 @@ __host__ __device__ inline uint32_t hash_step(uint32_t h, uint32_t x) {
 }
 
 // ---- workspace ----
-// [0, 256): status word; then o_part fp32 [max_splits, h_q, 512]; then
+// [0, 256): status word; then o_part fp32 [max_splits][64][h_q][8] (opart_index); then
 // lse_part fp32 [max_splits, h_q]; then the exact-recompute flags uint32
 // [vreq][4]: one bit per head (h_q <= 128), set by the decode kernel for a row
 // it could not certify and cleared by the combine kernel once it has
 // recomputed that row exactly (zero between calls)
 constexpr size_t kWsHeader = 256;
+// o_part element (split, head h, dim d): [split][64 units of 8 dims][h_q][8],
+// so that a warp of consecutive heads stores one unit as one contiguous run
+// (1 KB for 32 heads) and the combine reads 16 heads' unit as 512 B
+__host__ __device__ inline int64_t opart_index(int64_t split, int h_q, int h, int d) {
+  return ((split * 64 + (d >> 3)) * h_q + h) * 8 + (d & 7);
+}
 __host__ __device__ inline int64_t max_splits(int vreq, int parts) { return (int64_t)vreq + parts; }
 __host__ __device__ inline size_t ws_flags_offset(int vreq, int parts, int h_q) {
   const int64_t S = max_splits(vreq, parts);
@@ -70,7 +76,7 @@ struct DecodeParams {
   const int32_t* split_off;
   void* out;                   // [batch, s_q, h_q, 512], q dtype
   float* lse;                  // [batch, s_q, h_q]
-  float* o_part;               // [max_splits, h_q, 512]
+  float* o_part;               // [max_splits][64 units][h_q][8] (opart_index)
   float* lse_part;             // [max_splits, h_q]
   uint32_t* status;
   uint32_t* exact_flags;       // [vreq][4] head bits of rows to recompute exactly

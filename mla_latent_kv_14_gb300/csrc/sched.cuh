@@ -481,11 +481,9 @@ __device__ void exact_head(const CombineParams& p, int b, int i, int h) {
 }
 
 // Merge the split partials of each virtual request. grid = (vreq, h_q/16),
-// block = 256: each warp merges two heads, each lane 16 of the 512 dims.
+// block = 256: 16 heads per block, each thread 32 of one head's 512 dims.
 // Requests with a single piece were finished by the decode kernel; requests
-// with no visible token get out = 0, lse = -inf here. Lane s holds the lse
-// (and weight) of split s, so the weights take one load; the partial rows of
-// two splits are in flight at a time.
+// with no visible token get out = 0, lse = -inf here.
 template <typename OutT>
 __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   pdl_launch_dependents();  // a following schedule kernel may launch; it waits for this grid
@@ -508,68 +506,58 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   const int off = p.split_off[v];
   const int ns = p.split_off[v + 1] - off;
   if (ns == 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = blockIdx.y * 16 + warp * 2 + hh;
-    if (h >= p.h_q) break;
-    if ((fmask >> (warp * 2 + hh)) & 1u) continue;  // recomputed above
-    const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
-    OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
-    auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };
-    float mx = -INFINITY;
-    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, lse_at(s));
+  // Thread t merges, for head 16*blockIdx.y + hl, four dims of each of 8
+  // units of 8 dims: units 8*ug .. 8*ug+7, dims 4*half .. 4*half+3 of each.
+  // The 32 threads of a warp then read one unit of 16 heads, 512 contiguous
+  // bytes of the o_part layout (opart_index).
+  const int t = threadIdx.x;
+  const int hl = (t >> 1) & 15, half = t & 1, ug = t >> 5;
+  const int h = blockIdx.y * 16 + hl;
+  if (h >= p.h_q || ((fmask >> hl) & 1u)) return;  // recomputed above
+  const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
+  OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
+  auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };
+  float mx = -INFINITY;
+  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lse_at(s));
+  float4 acc[8];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float acc[16];
+  for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float ls = lse_at(s);
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - mx);
+      wsum += w;
+      const float* src = p.o_part + opart_index(off + s, p.h_q, h, 0) + 4 * half;
+      float4 x[8];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      for (int s0 = 0; s0 < ns; s0 += 32) {
-        const float ls = s0 + lane < ns ? lse_at(s0 + lane) : -INFINITY;
-        const float w_l = ls == -INFINITY ? 0.f : expf(ls - mx);
-        const int cnt = ns - s0 < 32 ? ns - s0 : 32;
-        for (int k = 0; k < cnt; k += 2) {
-          const bool two = k + 1 < cnt;
-          const float4* sa = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k) * p.h_q + h) * kDV);
-          const float4* sbp = reinterpret_cast<const float4*>(p.o_part + ((int64_t)(off + s0 + k + (two ? 1 : 0)) * p.h_q + h) * kDV);
-          float4 xa[4], xb[4];
+      for (int k = 0; k < 8; ++k)  // consecutive units are h_q * 8 floats apart
+        x[k] = *reinterpret_cast<const float4*>(src + (int64_t)(8 * ug + k) * p.h_q * 8);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            xa[j] = sa[j * 32 + lane];
-            xb[j] = sbp[j * 32 + lane];
-          }
-          const float wa = __shfl_sync(0xffffffffu, w_l, k);
-          const float wb = two ? __shfl_sync(0xffffffffu, w_l, (k + 1) & 31) : 0.f;
-          wsum += wa + wb;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[4 * j + 0] += wa * xa[j].x + wb * xb[j].x;
-            acc[4 * j + 1] += wa * xa[j].y + wb * xb[j].y;
-            acc[4 * j + 2] += wa * xa[j].z + wb * xb[j].z;
-            acc[4 * j + 3] += wa * xa[j].w + wb * xb[j].w;
-          }
-        }
+      for (int k = 0; k < 8; ++k) {
+        acc[k].x += w * x[k].x;
+        acc[k].y += w * x[k].y;
+        acc[k].z += w * x[k].z;
+        acc[k].w += w * x[k].w;
       }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int d = j * 128 + lane * 4;
-      if constexpr (sizeof(OutT) == 2) {
-        uint32_t lo, hi;
-        if constexpr (std::is_same<OutT, __half>::value) {
-          lo = pack_f16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
-          hi = pack_f16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
-        } else {
-          lo = pack_bf16x2(acc[4 * j] * inv, acc[4 * j + 1] * inv);
-          hi = pack_bf16x2(acc[4 * j + 2] * inv, acc[4 * j + 3] * inv);
-        }
-        *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
-      }
-    }
-    if (lane == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int d = 8 * (8 * ug + k) + 4 * half;
+    uint32_t lo, hi;
+    if constexpr (std::is_same<OutT, __half>::value) {
+      lo = pack_f16x2(acc[k].x * inv, acc[k].y * inv);
+      hi = pack_f16x2(acc[k].z * inv, acc[k].w * inv);
+    } else {
+      lo = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+      hi = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+    }
+    *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
+  }
+  if (ug == 0 && half == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace mla
