@@ -445,7 +445,9 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     c.scale_log2 = p.scale_log2;
   }
   cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, 1);
+  // 16 heads: 8 blocks per request share its 64 output units (no row is
+  // flagged for an exact recompute there, which every block would repeat)
+  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, c.exact_flags == nullptr && h_q <= 16 ? 8 : 1);
   cc.blockDim = dim3(256, 1, 1);
   cc.stream = st;
   cudaLaunchAttribute at[1];

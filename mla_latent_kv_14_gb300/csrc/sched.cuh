@@ -506,12 +506,16 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   const int off = p.split_off[v];
   const int ns = p.split_off[v + 1] - off;
   if (ns == 1) return;
-  // Thread t merges, for head 16*blockIdx.y + hl, four dims of each of 8
-  // units of 8 dims: units 8*ug .. 8*ug+7, dims 4*half .. 4*half+3 of each.
-  // The 32 threads of a warp then read one unit of 16 heads, 512 contiguous
-  // bytes of the o_part layout (opart_index).
+  // Thread t merges, for head 16*blockIdx.y + hl, four dims (4*half ..
+  // 4*half+3) of each of nu units of 8 dims, units u0 .. u0+nu-1. The 32
+  // threads of a warp then read one unit of 16 heads, 512 contiguous bytes of
+  // the o_part layout (opart_index). gridDim.z blocks share a request's 64
+  // units (more blocks when there are few heads; 1 whenever rows may be
+  // flagged for the exact recompute above, which each block would redo).
   const int t = threadIdx.x;
   const int hl = (t >> 1) & 15, half = t & 1, ug = t >> 5;
+  const int nu = 8 / (int)gridDim.z;
+  const int u0 = (8 * (int)blockIdx.z + ug) * nu;
   const int h = blockIdx.y * 16 + hl;
   if (h >= p.h_q || ((fmask >> hl) & 1u)) return;  // recomputed above
   const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
@@ -533,9 +537,10 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
       float4 x[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)  // consecutive units are h_q * 8 floats apart
-        x[k] = *reinterpret_cast<const float4*>(src + (int64_t)(8 * ug + k) * p.h_q * 8);
+        if (k < nu) x[k] = *reinterpret_cast<const float4*>(src + (int64_t)(u0 + k) * p.h_q * 8);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
+        if (k >= nu) break;
         acc[k].x += w * x[k].x;
         acc[k].y += w * x[k].y;
         acc[k].z += w * x[k].z;
@@ -546,7 +551,8 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const int d = 8 * (8 * ug + k) + 4 * half;
+    if (k >= nu) break;
+    const int d = 8 * (u0 + k) + 4 * half;
     uint32_t lo, hi;
     if constexpr (std::is_same<OutT, __half>::value) {
       lo = pack_f16x2(acc[k].x * inv, acc[k].y * inv);
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
     }
     *reinterpret_cast<uint2*>(orow + d) = make_uint2(lo, hi);
   }
-  if (ug == 0 && half == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+  if (u0 == 0 && half == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace mla
