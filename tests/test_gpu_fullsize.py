@@ -112,3 +112,47 @@ def test_fp8_sparse_full_size_sampled(workload):
         ro, rl = oracle.attend(oracle.to_f64(case.q[b, i].cpu()), oracle.dequantize_kv_fp8(raw_ref),
                                case.softmax_scale)
         assert_close_attn(out[b, i], lse[b, i], ro, rl, f"{workload} b={b} i={i}")
+
+
+@pytest.mark.parametrize("workload", ["v41_fp8_dense_b16_l32768", "v41_fp4_dense_b16_l32768",
+                                      "v41_fp8_sparse_b32_sq1_topk32768", "v41_fp4_sparse_b32_sq1_topk32768",
+                                      "v41_fp8_sparse_b32_sq1_topk2048", "v41_fp4_sparse_b32_sq1_topk2048"])
+def test_v41_full_size_sampled(workload):
+    """The V4.1 rows of 512 values (528-byte FP8, 288-byte FP4) at the
+    benchmark's sizes: the library's rows of the sampled requests equal the
+    oracle's quantisation byte for byte, and the oracle attends over their
+    dequantised values."""
+    w = bench.WORKLOADS[workload]
+    fmt, row_bytes, d_k, qname, dqname = bench.FORMATS[bench.workload_format(w)]
+    oq = getattr(oracle, qname[len("mla_"):])          # mla_quantize_kv_* -> quantize_kv_*
+    odq = getattr(oracle, dqname)
+    case, seqlens = bench.build_case(w, DEV)
+    raw = getattr(mla, qname)(case.kv_rows)
+    if w["kind"] == "sparse":
+        idx = case.indices.to(DEV)
+        meta, ns = mla.mla_get_metadata(None, 1, 128, batch=case.batch, topk=idx.shape[-1], kv_format=fmt,
+                                        device=DEV)
+        kv, bt, sl = raw.view(-1, 64, 1, row_bytes), None, None
+    else:
+        idx = None
+        bt, sl = case.block_table.to(DEV), case.cache_seqlens.to(DEV)
+        meta, ns = mla.mla_get_metadata(sl, 1, 128, kv_format=fmt)
+        kv = raw.view(case.num_blocks, 64, 1, row_bytes)
+    mla.mla_read_status(device=DEV)
+    out, lse = mla.mla_decode_with_kvcache(case.q, kv, bt, sl, 512, meta, ns, softmax_scale=case.softmax_scale,
+                                           kv_format=fmt, indices=idx)
+    torch.cuda.synchronize()
+    st, bits = mla.mla_read_status(device=DEV)
+    assert st == 0, f"device status {st} bits {bits}"
+    assert case.q.shape[-1] == d_k == 512
+    for b, i in _samples(case.batch, 1, n=3):
+        if idx is not None:
+            sel = case.indices.numpy()[b, i]
+            rows = sel[sel != -1].astype(np.int64)
+        else:
+            rows = synth.paged_rows_index(case.block_table.numpy()[b], int(seqlens[b]), case.page_block)
+        ridx = torch.from_numpy(rows).to(DEV)
+        raw_ref = oq(case.kv_rows[ridx].cpu())
+        assert (raw[ridx].cpu().numpy() == raw_ref).all(), "quantised rows differ"
+        ro, rl = oracle.attend(oracle.to_f64(case.q[b, i].cpu()), odq(raw_ref), case.softmax_scale)
+        assert_close_attn(out[b, i], lse[b, i], ro, rl, f"{workload} b={b} i={i}")

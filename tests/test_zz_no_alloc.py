@@ -76,3 +76,22 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
         mla.mla_decode_with_kvcache_noalloc(case.q.to(dev), case.kvcache_paged().to(dev), case.block_table.to(dev),
                                             sl, 512, meta, ns)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("fmt,row", [(mla.KV_FP8_528, 528), (mla.KV_FP4_288, 288)])
+def test_noalloc_v41_sparse_matches_regular_entry(fmt, row):
+    """The V4.1 rows (kv_format 2 and 3), token-sparse, through both entry points."""
+    dev = "cuda"
+    case = synth.make_sparse_case(3, 2, 192, tokens_per_request=1024, seed=63, d_k=512)
+    quant = mla.mla_quantize_kv_fp8_528 if fmt == mla.KV_FP8_528 else mla.mla_quantize_kv_fp4_288
+    kv = quant(case.kv_rows.to(dev)).view(-1, 64, 1, row)
+    q, idx = case.q.to(dev), case.indices.to(dev)
+    meta, ns = mla.mla_get_metadata(None, 2, 128, batch=3, topk=192, kv_format=fmt, device=dev)
+    ref_o, ref_l = mla.mla_decode_with_kvcache(q, kv, None, None, 512, meta, ns, softmax_scale=case.softmax_scale,
+                                               kv_format=fmt, indices=idx)
+    status = torch.full((1,), 0xFFFF, dtype=torch.int32, device=dev)
+    o, l = mla.mla_decode_with_kvcache_noalloc(q, kv, None, None, 512, meta, ns, softmax_scale=case.softmax_scale,
+                                               kv_format=fmt, indices=idx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close_attn(o, l, ref_o.float().cpu().numpy(), ref_l.cpu().numpy(), "noalloc vs regular, V4.1")
