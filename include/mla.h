@@ -48,7 +48,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,      /* bad shape, pointer, alignment or flag combination */
-  MLA_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement */
+  MLA_ERR_UNSUPPORTED = 2,      /* valid request the library does not implement   */
   MLA_ERR_STALE_METADATA = 3,   /* metadata computed for a different shape/lengths */
   MLA_ERR_INDEX = 4,            /* an out-of-range page or sparse index was skipped */
   MLA_ERR_TIMEOUT = 5,          /* a device pipeline wait gave up (kernel returned early) */
