@@ -1,10 +1,13 @@
-// decode_dense.cuh -- MLA decode over a paged BF16/FP16 latent cache, sm_103a.
+// decode_dense.cuh -- MLA decode, 128 heads, over a latent cache of 16-bit,
+// 656-byte FP8 or V4.1 (528-byte FP8, 288-byte FP4) rows, read through a block
+// table or an index list, sm_103a.
 //
 // What one 2-CTA cluster computes. A persistent cluster owns one range of the
 // split-KV schedule (a list of (virtual request, tile range) pieces). For a
 // piece it keeps, for all 128 heads, the online-softmax state (m, l) and the
 // 512-wide latent output O, and walks the piece's 64-token tiles:
-//   S  = Q K^T              (128 heads x 64 tokens, contraction over 576)
+//   S  = Q K^T              (128 heads x 64 tokens, contraction over 576, or
+//                            512 for the V4.1 rows)
 //   P  = exp(S*scale - m)   (online softmax with running max / sum)
 //   O += P V                (V = the first 512 dims of the same rows)
 // ("矩阵、注意力与 GPU：拆解 DeepGEMM 与 FlashMLA", §五 flashDecode, §六 absorbed MQA
@@ -28,7 +31,7 @@
 // products sum to at least 2^8 is therefore certified to within 2^-12; that
 // fails only when the two halves' scores disagree by more than about 22
 // binades. Such a row is flagged and the combine kernel recomputes it exactly
-// (16-bit caches) or it is reported as out of range (FP8 caches). No tensor-core work is
+// (16-bit caches) or it is reported as out of range (quantised rows). No tensor-core work is
 // duplicated and no KV byte is read twice; the exchange is 16.5 KB per tile
 // and direction. (Prior art on the pages: the Hopper kernel splits O between
 // two warpgroups -- seesaw -- because the register file is full, and the FP8
@@ -44,16 +47,17 @@
 // the copy, the CTA's 32 RoPE dims of Q (8 KB) and a ring of KV tiles (36 KB
 // each: four 64-wide latent chunks, 128-byte swizzled, loaded as one 3-D TMA
 // box, and one 32-wide RoPE chunk, 64-byte swizzled): 5 slots for 16-bit
-// caches; 3 for FP8 caches, whose raw e4m3 rows and scales stage in 3 more
-// slots (dense: TMA; sparse: TMA gather4, four rows per copy, with the RoPE
-// dims gathered straight into the operand slot).
+// caches; 3 for quantised rows (32 KB without the RoPE chunk for the V4.1
+// rows), whose raw codes, scales and (656-byte rows) RoPE dims stage in 3 more
+// slots (dense: TMA; sparse: TMA gather4, four rows per copy); the dequant
+// warps fill the operand slot from them.
 //
 // Warp roles. Warp 0: producer (TMA; the whole warp in the sparse mode).
-// Warp 1: owns TMEM; lane 0 issues QK^T. Warp kPvWarp (2, or 14 for FP8
-// caches): lane 0 issues P . V, so a P . V never waits behind the issue of a
+// Warp 1: owns TMEM; lane 0 issues QK^T. Warp kPvWarp (2, or 14 for quantised
+// rows): lane 0 issues P . V, so a P . V never waits behind the issue of a
 // QK^T tile; it holds a ready P . V back while a QK^T is executing, so that
 // it fills the pipe while the E warps read S instead of delaying S. Warps 2-3
-// and 12-13 (FP8 caches): e4m3 x scale -> fp16 operand tiles. Warps 4-7 (E):
+// and 12-13 (quantised rows): codes x scale -> fp16 operand tiles. Warps 4-7 (E):
 // read S, form E_r and the row max, stage them and send them to the peer with
 // one bulk shared-to-shared copy; they also copy each piece's Q rows into
 // TMEM. Warps 8-11 (P): receive the peer's message, form P into TMEM, rescale
@@ -63,7 +67,7 @@
 //
 // Pipeline. Every hand-off is an mbarrier; every wait is bounded (a wait that
 // gives up sets a status bit and the kernel unwinds). Measured on GB300 with
-// per-tile clock stamps: the tile period (about 2,300 cycles for 16-bit
+// per-tile clock stamps: the tile period (about 2,150 cycles for 16-bit
 // caches) is set by two loops of about that length -- QK^T issue and
 // completion plus the E warps' read of the single S buffer, and the exchange
 // buffers (a 16.5 KB copy between the SMs of a pair lands about 1,250 cycles
@@ -93,10 +97,10 @@ enum : int {
 constexpr int kKChunk = 64 * 128;          // 64 tokens x 64 x 2 B
 constexpr int kRChunk = 64 * 64;           // 64 tokens x 32 RoPE dims x 2 B
 constexpr int kSlot = 4 * kKChunk + kRChunk;
-constexpr int kThreads = 384;              // 16-bit caches (FP8 caches: Cfg::kThreads)
+constexpr int kThreads = 384;              // 16-bit caches (quantised rows: Cfg::kThreads)
 constexpr int kEWarps = 4;                 // warps 4-7: exponentiate and send
 constexpr int kPWarps = 4;                 // warps 8-11: receive, form P, epilogue
-constexpr int kDequantWarps = 4;           // warps 2-3 and 12-13 (FP8 caches)
+constexpr int kDequantWarps = 4;           // warps 2-3 and 12-13 (quantised rows)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;            // S at columns 256..319 (one buffer)
 constexpr uint32_t kColP = 320;            // P of tile g: 16-bit pairs at columns 320 + 32*(g&1)
@@ -931,7 +935,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kMode>::kThreads
         }
         if (!kQuant && vm != ~0ull) {
           // zero the V rows of masked tokens: 0 * (whatever is there) must not
-          // turn into NaN inside P . V (the dequant warps do this for FP8 rows)
+          // turn into NaN inside P . V (the dequant warps do this for quantised rows)
           const uint32_t slot = sb + C::OFF_RING + (g % NS) * C::kSlotBytes;
           for (int e2 = pid; e2 < 64 * 32; e2 += 128) {
             const int row = e2 >> 5, u = e2 & 31;

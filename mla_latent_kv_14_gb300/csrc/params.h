@@ -67,11 +67,11 @@ struct MetaParams {
 };
 
 struct DecodeParams {
-  const void* q;               // [batch, s_q, h_q, 576]
+  const void* q;               // [batch, s_q, h_q, 576] (512 for the V4.1 rows)
   const int32_t* block_table;  // [batch, max_blocks] (dense)
   const int32_t* seqlens;      // [batch]
   const int32_t* indices;      // [batch, s_q, topk] (sparse) or null
-  const uint8_t* kv;           // the cache rows as bytes (1152-B 16-bit or 656-B FP8 rows)
+  const uint8_t* kv;           // the cache rows as bytes (1152-B 16-bit, or 656-, 528- or 288-B quantised rows)
   const int32_t* meta;
   const int32_t* split_off;
   void* out;                   // [batch, s_q, h_q, 512], q dtype
