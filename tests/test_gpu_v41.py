@@ -328,3 +328,27 @@ def test_split_peaks(name, delta):
     assert st == 0, (st, bits)
     ro, rl = _oracle_dense(case, raw, f)
     assert_close_attn(out, lse, ro, rl, f"{name} split peaks delta={delta}")
+
+
+@pytest.mark.parametrize("name", list(FORMATS))
+def test_split_and_combine_entry_points(name):
+    """mla_decode_splitkv followed by mla_combine_splits equals the one-call
+    decode for the V4.1 rows (requests cut into pieces by parts = 3)."""
+    f = FORMATS[name]
+    case = synth.make_dense_case([300, 77, 1], seed=101, d_k=512)
+    raw = f["quant"](case.kv_rows.to(DEV))
+    sl, bt = case.cache_seqlens.to(DEV), case.block_table.to(DEV)
+    kv = raw.view(case.num_blocks, 64, 1, f["row"])
+    q = case.q.to(DEV)
+    meta, ns = _meta(sl, 1, f["fmt"], parts=3)
+    kw = dict(softmax_scale=case.softmax_scale, kv_format=f["fmt"])
+    mla.mla_read_status(device=DEV)
+    o1, l1 = mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, meta, ns, **kw)
+    o2 = torch.empty_like(o1)
+    l2 = torch.empty_like(l1)
+    mla.mla_decode_splitkv(q, kv, bt, sl, 512, meta, ns, out=o2, lse=l2, **kw)
+    mla.mla_combine_splits(q, kv, bt, sl, 512, meta, ns, out=o2, lse=l2, **kw)
+    torch.cuda.synchronize()
+    st, bits = mla.mla_read_status(device=DEV)
+    assert st == 0, (st, bits)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
