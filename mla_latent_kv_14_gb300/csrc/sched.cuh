@@ -490,6 +490,9 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   pdl_wait();  // the decode grid has completed and its writes are visible
   const int v = blockIdx.x;
   const int b = v % p.batch, i = v / p.batch;
+  // the request's split range and its flag word are loaded together
+  const int off = p.split_off[v];
+  const int ns = p.split_off[v + 1] - off;
   // rows the decode kernel flagged (bit k: head 16*blockIdx.y + k) are
   // recomputed exactly and left out of the merge below; their bits are cleared
   uint32_t fmask = 0u;
@@ -503,8 +506,6 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
       if (threadIdx.x == 0) atomicAnd(fw, ~(0xFFFFu << (h0 & 31)));
     }
   }
-  const int off = p.split_off[v];
-  const int ns = p.split_off[v + 1] - off;
   if (ns == 1) return;
   // Thread t merges, for head 16*blockIdx.y + hl, four dims (4*half ..
   // 4*half+3) of each of nu units of 8 dims, units u0 .. u0+nu-1. The 32
@@ -520,32 +521,52 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   if (h >= p.h_q || ((fmask >> hl) & 1u)) return;  // recomputed above
   const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
   OutT* orow = reinterpret_cast<OutT*>(p.out) + row * kDV;
-  auto lse_at = [&](int s) { return p.lse_part[(int64_t)(off + s) * p.h_q + h]; };
-  float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lse_at(s));
+  const int64_t ustride = (int64_t)p.h_q * 8;  // floats from one unit to the next
+  const int64_t sstride = 64 * ustride;        // and from one split to the next
+  const float* src = p.o_part + opart_index(off, p.h_q, h, 8 * u0) + 4 * half;
+  const float* lsp = p.lse_part + (int64_t)off * p.h_q + h;
+  // The first two pieces' partials are loaded together with every piece's
+  // lse, so that a request cut once costs one round trip to memory.
+  float4 x0[8], x1[8];
+  float l0 = -INFINITY, l1 = -INFINITY, mx = -INFINITY;
+  if (ns >= 2) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < nu) {
+        x0[k] = *reinterpret_cast<const float4*>(src + k * ustride);
+        x1[k] = *reinterpret_cast<const float4*>(src + sstride + k * ustride);
+      }
+    l0 = lsp[0];
+    l1 = lsp[p.h_q];
+    mx = fmaxf(l0, l1);
+    for (int s = 2; s < ns; ++s) mx = fmaxf(mx, lsp[(int64_t)s * p.h_q]);
+  }
   float4 acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float ls = lse_at(s);
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - mx);
-      wsum += w;
-      const float* src = p.o_part + opart_index(off + s, p.h_q, h, 0) + 4 * half;
-      float4 x[8];
+  // o += e^{lse_s - m} o_s, in the order of the pieces
+  auto add = [&](const float4(&x)[8], float ls) {
+    if (ls == -INFINITY) return;  // an empty piece (m is finite otherwise)
+    const float w = expf(ls - mx);
+    wsum += w;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)  // consecutive units are h_q * 8 floats apart
-        if (k < nu) x[k] = *reinterpret_cast<const float4*>(src + (int64_t)(u0 + k) * p.h_q * 8);
+    for (int k = 0; k < 8; ++k) {
+      if (k >= nu) break;
+      acc[k].x += w * x[k].x;
+      acc[k].y += w * x[k].y;
+      acc[k].z += w * x[k].z;
+      acc[k].w += w * x[k].w;
+    }
+  };
+  if (ns >= 2) {
+    add(x0, l0);
+    add(x1, l1);
+    for (int s = 2; s < ns; ++s) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k >= nu) break;
-        acc[k].x += w * x[k].x;
-        acc[k].y += w * x[k].y;
-        acc[k].z += w * x[k].z;
-        acc[k].w += w * x[k].w;
-      }
+      for (int k = 0; k < 8; ++k)
+        if (k < nu) x0[k] = *reinterpret_cast<const float4*>(src + s * sstride + k * ustride);
+      add(x0, lsp[(int64_t)s * p.h_q]);
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
