@@ -12,7 +12,7 @@ constexpr int kRowBytesFp8 = 656;
 constexpr int kDV41 = 512;        // V4.1 rows: 512 values (latent and RoPE together)
 constexpr int kRowBytesFp8_528 = 528;
 constexpr int kRowBytesFp4_288 = 288;
-constexpr int kPieceOverhead = 2; // schedule cost of starting a piece, in tiles
+constexpr int kPieceOverhead = 5; // schedule cost of starting a request, in tiles
 
 // ---- metadata (int32 words) ----
 // header
