@@ -12,7 +12,11 @@ constexpr int kRowBytesFp8 = 656;
 constexpr int kDV41 = 512;        // V4.1 rows: 512 values (latent and RoPE together)
 constexpr int kRowBytesFp8_528 = 528;
 constexpr int kRowBytesFp4_288 = 288;
-constexpr int kPieceOverhead = 5; // schedule cost of starting a request, in tiles
+// schedule cost of starting a request, in tiles: a piece switch of the
+// 128-head kernel (a 256 KB epilogue, the next query, refilling the pair's
+// pipeline) costs more than one of the 16-head kernel
+constexpr int kPieceOverhead = 5;
+constexpr int kPieceOverheadFewHeads = 2;
 
 // ---- metadata (int32 words) ----
 // header

@@ -91,11 +91,12 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 }
 
 // The schedule as a closed form, computed by one block:
-//  * request v costs n_v + kPieceOverhead (0 if it has no tile); C_v is the
-//    exclusive prefix sum of the costs and `total` their sum;
+//  * request v costs n_v + ov (0 if it has no tile), ov = kPieceOverhead
+//    (kPieceOverheadFewHeads for 16 heads); C_v is the exclusive prefix sum
+//    of the costs and `total` their sum;
 //  * part p owns the cost interval [p*per, (p+1)*per), per = ceil(total/parts)
-//    (at least kPieceOverhead + 1); position x maps to the tile cursor
-//    (v, max(0, x - C_v - kPieceOverhead)) of the request whose cost interval
+//    (at least ov + 1); position x maps to the tile cursor
+//    (v, max(0, x - C_v - ov)) of the request whose cost interval
 //    holds x, so a part runs from cursor(p*per) to cursor((p+1)*per);
 //  * a request is cut once per part boundary that falls on one of its tiles
 //    other than its first.
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p
   int* firstp = nsplit + V;                                 // [V]
   __shared__ long long warp_tot[33];
   __shared__ long long carry;
+  const int ov = p.h_q == 128 ? kPieceOverhead : kPieceOverheadFewHeads;
   if (threadIdx.x == 0) carry = 0;
   for (int v = threadIdx.x; v < V; v += blockDim.x) {
     int L;
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p
   __syncthreads();
   for (int base = 0; base < V; base += blockDim.x) {
     const int v = base + threadIdx.x;
-    const long long c = v < V && n[v] ? (long long)n[v] + kPieceOverhead : 0;
+    const long long c = v < V && n[v] ? (long long)n[v] + ov : 0;
     long long excl;
     const long long tot = block_exclusive_scan(c, warp_tot, excl);
     if (v < V) C[v] = carry + excl;
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p
   if (threadIdx.x == 0) C[V] = total;
   __syncthreads();
   long long per = total > 0 ? (total + p.parts - 1) / p.parts : 1;
-  if (per < kPieceOverhead + 1) per = kPieceOverhead + 1;
+  if (per < ov + 1) per = ov + 1;
   auto cursor = [&](long long x, int& cv, int& ct) {
     if (x >= total) { cv = V; ct = 0; return; }
     int lo = 0, hi = V - 1;                 // largest v with C[v] <= x
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(MetaParams p
       if (C[mid] <= x) lo = mid; else hi = mid - 1;
     }
     cv = lo;
-    const long long t = x - C[lo] - kPieceOverhead;
+    const long long t = x - C[lo] - ov;
     ct = t > 0 ? (int)t : 0;
   };
   // part boundaries that cut a request
