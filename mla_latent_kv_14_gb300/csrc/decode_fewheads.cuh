@@ -18,12 +18,12 @@
 // one TMA box of 72 KB), Q of the piece (9 chunks of 64 dims x 16 heads), two
 // P^T buffers ([16 heads][64 tokens], 128-B swizzled), reduction scratch.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and lane
-// 0 issues UMMA; warps 2-5 are the softmax warps, warp w serving TMEM lanes
-// 32*(w%4) .. +31. An M=64 accumulator keeps its rows in lanes 0-15 of each
-// 32-lane quarter, so softmax thread (quarter q, lane < 16) holds token 16q +
-// lane of the tile with its 16 head scores; for the 128-row O^T blocks every
-// lane is one output dim.
+// Warp roles (224 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and lane
+// 0 issues S^T; lane 0 of warp 6 issues P . V; warps 2-5 are the softmax
+// warps, warp w serving TMEM lanes 32*(w%4) .. +31. An M=64 accumulator keeps
+// its rows in lanes 0-15 of each 32-lane quarter, so softmax thread (quarter
+// q, lane < 16) holds token 16q + lane of the tile with its 16 head scores;
+// for the 128-row O^T blocks every lane is one output dim.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -36,8 +36,9 @@ namespace mla {
 namespace few {
 
 constexpr int kNH = 16;                       // heads
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kSoftWarps = 4;                 // warps 2-5
+constexpr int kPvWarp = 6;                    // its lane 0 issues P . V
 constexpr int kChunks = 9;                    // 576 = 9 x 64 dims
 constexpr uint32_t kChunkBytes = 64 * 128;    // 64 tokens x 64 dims x 2 B
 constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
@@ -57,7 +58,7 @@ constexpr uint32_t OFF_BAR = OFF_RED + kSoftWarps * kNH * 4;
 enum : uint32_t {
   B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
   B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2, B_OEMPTY = B_PEMPTY + 2,
-  B_DRAIN = B_OEMPTY + 1, B_STALL = B_DRAIN + 1, B_COUNT = B_STALL + 1
+  B_DRAIN = B_OEMPTY + 1, B_DRAIN2 = B_DRAIN + 1, B_STALL = B_DRAIN2 + 1, B_COUNT = B_STALL + 1
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_OEMPTY), kSoftWarps);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN2), 1);
     mbar_init(bar(B_STALL), 1);
     *abort_flag = 0u;
   }
@@ -167,47 +169,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t t_0 = cycles();
       while (!mbar_try_wait(bar(B_QFULL), q_last & 1) && cycles() - t_0 < kDrainLimitCycles) {}
     }
-  } else if (ok && warp == 1 && lane == 0) {
-    // ---------------- UMMA issuer ----------------
+  } else if (ok && lane == 0 && (warp == 1 || warp == kPvWarp)) {
+    // ---------------- UMMA issue: S^T by warp 1, P . V by warp kPvWarp ----------------
+    // Two issuing threads, each waiting only on its own inputs, so that a
+    // ready P . V never waits behind the issue of a tile's 36 S^T MMAs.
     constexpr uint32_t idesc_qk = idesc_f16(64, kNH, !kFp16, false, false);   // K tile (tokens x dims), Q (heads x dims)
     constexpr uint32_t idesc_pv = idesc_f16(128, kNH, !kFp16, true, false);   // V^T (dims-major), P^T (heads x tokens)
     PieceIter it(p, part);
     Piece pc;
-    bool have = it.next(pc);
-    int qk_t = have ? pc.t0 : 0, qk_g = 0, pv_g = 0, k_piece = 0;
-    bool q_ready = false;
-    uint32_t first_bits = 0;
-    int piece_of[4] = {0, 0, 0, 0};
-    uint64_t t_last = 0;
-    int idle = 0;
-    while (true) {
-      bool progressed = false;
-      if (pv_g < qk_g && mbar_test(bar(B_PFULL + (pv_g & 1)), (pv_g >> 1) & 1)) {
-        const bool first = (first_bits >> (pv_g & 31)) & 1u;
-        const int pk = piece_of[pv_g & 3];
-        if (!first || pk == 0 || mbar_test(bar(B_OEMPTY), (pk - 1) & 1)) {
-          tc_fence_after();
-          const uint32_t slot = sb + OFF_RING + (pv_g % kNS) * kTileBytes;
-          const uint64_t d_p = sdesc_sw128(sb + OFF_P + (pv_g & 1) * kPBytes, 16, 1024);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // V^T block j: dims [128j, 128j+128) = chunks 2j, 2j+1; +128 per 16 tokens
-            const uint64_t d_v = sdesc_sw128(slot + 2 * j * kChunkBytes, kChunkBytes, 1024);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ss(tmem + kColO + 16u * j, d_v + 128u * k, d_p + 2u * k, idesc_pv, (first && k == 0) ? 0u : 1u);
+    int g = 0, k = 0;
+    bool failed = false;
+    uint32_t drain_bar = bar(B_DRAIN);
+    if (warp == 1) {
+      while (!failed && it.next(pc)) {
+        if (!wait(bar(B_QFULL), k & 1, guard)) break;
+        for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+          const int s = g % kNS, sbuf = g & 1;
+          if (!wait(bar(B_FULL + s), (g / kNS) & 1, guard) ||
+              !wait(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard)) {
+            failed = true;
+            break;
           }
-          umma_commit(bar(B_PEMPTY + (pv_g & 1)));
-          umma_commit(bar(B_EMPTY + pv_g % kNS));
-          ++pv_g;
-          progressed = true;
-        }
-      }
-      if (have) {
-        if (!q_ready && mbar_test(bar(B_QFULL), k_piece & 1)) q_ready = true;
-        const int s = qk_g % kNS, sbuf = qk_g & 1;
-        if (q_ready && mbar_test(bar(B_FULL + s), (qk_g / kNS) & 1) &&
-            mbar_test(bar(B_SEMPTY + sbuf), ((qk_g >> 1) & 1) ^ 1)) {
           tc_fence_after();
           const uint32_t slot = sb + OFF_RING + s * kTileBytes;
 #pragma unroll
@@ -215,46 +197,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t d_k = sdesc_sw128(slot + c * kChunkBytes, 16, 1024);
             const uint64_t d_q = sdesc_sw128(sb + OFF_Q + c * kQChunk, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ss(tmem + 16u * sbuf, d_k + 2u * k, d_q + 2u * k, idesc_qk, (c | k) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ss(tmem + 16u * sbuf, d_k + 2u * kk, d_q + 2u * kk, idesc_qk, (c | kk) ? 1u : 0u);
           }
           umma_commit(bar(B_SFULL + sbuf));
-          const bool first = qk_t == pc.t0;
-          first_bits = (first_bits & ~(1u << (qk_g & 31))) | ((first ? 1u : 0u) << (qk_g & 31));
-          piece_of[qk_g & 3] = k_piece;
-          ++qk_g;
-          if (++qk_t == pc.t1) {
-            umma_commit(bar(B_QEMPTY));
-            have = it.next(pc);
-            if (have) qk_t = pc.t0;
-            ++k_piece;
-            q_ready = false;
-          }
-          progressed = true;
         }
+        if (failed) break;
+        umma_commit(bar(B_QEMPTY));  // Q of the piece is free once its last S^T is done
+        ++k;
       }
-      if (!have && pv_g == qk_g) break;
-      // the wait limit is checked after every 64 idle polls
-      if (progressed) {
-        idle = 0;
-        t_last = 0;
-      } else if (++idle == 64) {
-        idle = 0;
-        if (*abort_flag) break;
-        const uint64_t now = cycles();
-        if (t_last == 0) {
-          t_last = now;
-        } else if (now - t_last > guard.limit) {
-          *abort_flag = 1u;
-          atomicOr(p.status, STATUS_TIMEOUT);
-          break;
+    } else {
+      drain_bar = bar(B_DRAIN2);
+      while (!failed && it.next(pc)) {
+        for (int t = pc.t0; t < pc.t1; ++t, ++g) {
+          // a piece's first P . V overwrites O^T: the previous piece's epilogue must have read it
+          if (!wait(bar(B_PFULL + (g & 1)), (g >> 1) & 1, guard) ||
+              (t == pc.t0 && k > 0 && !wait(bar(B_OEMPTY), (k - 1) & 1, guard))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const bool first = t == pc.t0;
+          const uint32_t slot = sb + OFF_RING + (g % kNS) * kTileBytes;
+          const uint64_t d_p = sdesc_sw128(sb + OFF_P + (g & 1) * kPBytes, 16, 1024);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // V^T block j: dims [128j, 128j+128) = chunks 2j, 2j+1; +128 per 16 tokens
+            const uint64_t d_v = sdesc_sw128(slot + 2 * j * kChunkBytes, kChunkBytes, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ss(tmem + kColO + 16u * j, d_v + 128u * kk, d_p + 2u * kk, idesc_pv, (first && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(bar(B_PEMPTY + (g & 1)));
+          umma_commit(bar(B_EMPTY + g % kNS));
         }
+        ++k;
       }
     }
-    umma_commit(bar(B_DRAIN));
+    // every UMMA this thread issued has completed before TMEM is released
+    umma_commit(drain_bar);
     const uint64_t t_0 = cycles();
-    while (!mbar_try_wait(bar(B_DRAIN), 0) && cycles() - t_0 < kDrainLimitCycles) {}
-  } else if (ok && warp >= 2) {
+    while (!mbar_try_wait(drain_bar, 0) && cycles() - t_0 < kDrainLimitCycles) {}
+  } else if (ok && warp >= 2 && warp < 2 + kSoftWarps) {
     // ---------------- softmax warps ----------------
     const int q4 = warp & 3;                              // TMEM lane quarter
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
