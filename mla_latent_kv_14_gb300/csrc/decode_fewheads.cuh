@@ -9,14 +9,19 @@
 //   O^T += V^T P^T     (512 dims x 16 heads, as four 128-dim blocks)
 // and the epilogue writes O^T / l transposed back into [head][dim] order.
 // The work is bound by the cache bytes (about 30 FLOP per byte), so one CTA
-// per SM streams 64-token tiles through a two-slot ring; no pairing is needed
-// because O^T is only 64 TMEM columns.
+// per SM streams 64-token tiles; no pairing is needed because O^T is only 64
+// TMEM columns. How many bytes each SM keeps in flight sets the rate, so the
+// ring is cut finer than a 72 KB tile: 11 units of two latent chunks (16 KB,
+// the V^T block of 128 dims that one P . V MMA reads) and 3 RoPE chunks (8 KB,
+// read only by S^T and freed as soon as it completes), 2.75 tiles in all,
+// where two whole-tile slots are all that fit beside Q and P.
 //
 // Memory map. TMEM (128 columns): S^T buffers [0,16) and [16,32), O^T blocks
-// [64 + 16j, 80 + 16j) for dims [128j, 128j+128). Shared memory: two ring slots
-// of one 64-token tile each (9 chunks of 64 dims x 64 tokens, 128-B swizzled:
-// one TMA box of 72 KB), Q of the piece (9 chunks of 64 dims x 16 heads), two
-// P^T buffers ([16 heads][64 tokens], 128-B swizzled), reduction scratch.
+// [64 + 16j, 80 + 16j) for dims [128j, 128j+128). Shared memory: the unit ring
+// (chunks of 64 dims x 64 tokens, 128-B swizzled; tile g's latent pair j is
+// unit (4g + j) mod 11, its RoPE chunk unit g mod 3), Q of the piece (9 chunks
+// of 64 dims x 16 heads), two P^T buffers ([16 heads][64 tokens], 128-B
+// swizzled), reduction scratch.
 //
 // Warp roles (224 threads): warp 0 lane 0 issues TMA; warp 1 owns TMEM and lane
 // 0 issues S^T; lane 0 of warp 6 issues P . V; warps 2-5 are the softmax
@@ -41,36 +46,49 @@ constexpr int kSoftWarps = 4;                 // warps 2-5
 constexpr int kPvWarp = 6;                    // its lane 0 issues P . V
 constexpr int kChunks = 9;                    // 576 = 9 x 64 dims
 constexpr uint32_t kChunkBytes = 64 * 128;    // 64 tokens x 64 dims x 2 B
-constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
 constexpr uint32_t kQChunk = kNH * 128;       // 16 heads x 64 dims x 2 B
 constexpr uint32_t kQBytes = kChunks * kQChunk;
 constexpr uint32_t kPBytes = kNH * 128;       // [16 heads][64 tokens] x 2 B
-constexpr int kNS = 2;
+constexpr int kPairs = 11;                    // ring units of two latent chunks (16 KB)
+constexpr int kRopes = 3;                     // ring units of one RoPE chunk (8 KB)
+constexpr uint32_t kPairBytes = 2 * kChunkBytes;
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kColO = 64;
 constexpr uint32_t kSoftBar = 1;              // named barrier of the 128 softmax threads
 
 constexpr uint32_t OFF_RING = 0;
-constexpr uint32_t OFF_Q = OFF_RING + kNS * kTileBytes;
+constexpr uint32_t OFF_ROPE = OFF_RING + kPairs * kPairBytes;
+constexpr uint32_t OFF_Q = OFF_ROPE + kRopes * kChunkBytes;
 constexpr uint32_t OFF_P = OFF_Q + kQBytes;
 constexpr uint32_t OFF_RED = OFF_P + 2 * kPBytes;          // [4 warps][16 heads] floats
 constexpr uint32_t OFF_BAR = OFF_RED + kSoftWarps * kNH * 4;
 enum : uint32_t {
-  B_FULL = 0, B_EMPTY = B_FULL + kNS, B_QFULL = B_EMPTY + kNS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
+  B_FULL = 0, B_EMPTY = B_FULL + kPairs, B_RFULL = B_EMPTY + kPairs, B_REMPTY = B_RFULL + kRopes,
+  B_QFULL = B_REMPTY + kRopes, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
   B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2, B_OEMPTY = B_PEMPTY + 2,
   B_DRAIN = B_OEMPTY + 1, B_DRAIN2 = B_DRAIN + 1, B_STALL = B_DRAIN2 + 1, B_COUNT = B_STALL + 1
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * B_COUNT;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64 + 1024;
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "128-B swizzled operands need 1024-B alignment");
+static_assert(OFF_ROPE % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0,
+              "128-B swizzled operands need 1024-B alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
+// ring unit n (n = 4g + j: latent chunks 2j, 2j+1 of tile g)
+__device__ __forceinline__ uint32_t pair_addr(uint32_t sb, int n) {
+  return sb + OFF_RING + (uint32_t)(n % kPairs) * kPairBytes;
+}
+// chunk c (0..8, 8 = RoPE) of tile g
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t sb, int g, int c) {
+  return c < 8 ? pair_addr(sb, 4 * g + (c >> 1)) + (uint32_t)(c & 1) * kChunkBytes
+               : sb + OFF_ROPE + (uint32_t)(g % kRopes) * kChunkBytes;
+}
 
 template <bool kFp16>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_decode_fewheads_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                               const DecodeParams p) {
+    mla_decode_fewheads_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k2,
+                               const __grid_constant__ CUtensorMap tm_k1, const DecodeParams p) {
   using OutT = typename std::conditional<kFp16, __half, __nv_bfloat16>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -85,9 +103,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Guard guard{abort_flag, p.status, kWaitLimitCycles};
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kPairs; ++s) {
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int s = 0; s < kRopes; ++s) {
+      mbar_init(bar(B_RFULL + s), 1);
+      mbar_init(bar(B_REMPTY + s), 1);
     }
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
@@ -129,14 +151,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok = *ok_flag != 0u;
 
   if (ok && warp == 0 && lane == 0) {
-    // ---------------- producer: Q per piece, one 72 KB box per tile ----------------
+    // ---------------- producer: Q per piece; per tile four latent pairs and the RoPE chunk ----------------
     prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_k2);
+    prefetch_tmap(&tm_k1);
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
     PieceIter it(p, part);
     Piece pc;
-    int g = 0, qn = 0, last_g[kNS] = {-1, -1}, q_last = -1;
+    int g = 0, qn = 0, q_last = -1;
+    int last_n[kPairs], last_r[kRopes];
+    for (int u = 0; u < kPairs; ++u) last_n[u] = -1;
+    for (int u = 0; u < kRopes; ++u) last_r[u] = -1;
     bool stop = false;
     auto raw_page = [&](int b, int t) {
       return t < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + t) : -1;
@@ -149,21 +175,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       q_last = qn++;
       int pg_next = raw_page(b, pc.t0);  // block-table entries are loaded one tile ahead
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-        const int s = g % kNS;
         int page = pg_next;
         page = (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the softmax warps
         pg_next = raw_page(b, t + 1);
-        if (!wait(bar(B_EMPTY + s), ((g / kNS) & 1) ^ 1, guard)) { stop = true; break; }
-        mbar_arrive_expect_tx(bar(B_FULL + s), kTileBytes);
-        tma_load_3d(sb + OFF_RING + s * kTileBytes, &tm_k, bar(B_FULL + s), 0, page * kTile, 0, pol_kv);
-        last_g[s] = g;
+        // in the order the units free up: the RoPE chunk (freed by S^T three
+        // tiles back), then latent pairs 0-2 (P . V three tiles back) and 3
+        // (P . V two tiles back)
+        const int r = g % kRopes;
+        if (!wait(bar(B_REMPTY + r), ((g / kRopes) & 1) ^ 1, guard)) { stop = true; break; }
+        mbar_arrive_expect_tx(bar(B_RFULL + r), kChunkBytes);
+        tma_load_3d(sb + OFF_ROPE + r * kChunkBytes, &tm_k1, bar(B_RFULL + r), 0, page * kTile, 8, pol_kv);
+        last_r[r] = g;
+        for (int j = 0; j < 4 && !stop; ++j) {  // latent chunks 2j, 2j+1: one 16 KB box
+          const int n = 4 * g + j, u = n % kPairs;
+          if (!wait(bar(B_EMPTY + u), ((n / kPairs) & 1) ^ 1, guard)) { stop = true; break; }
+          mbar_arrive_expect_tx(bar(B_FULL + u), kPairBytes);
+          tma_load_3d(sb + OFF_RING + u * kPairBytes, &tm_k2, bar(B_FULL + u), 0, page * kTile, 2 * j, pol_kv);
+          last_n[u] = n;
+        }
+        if (stop) break;
       }
     }
     // never leave with a copy in flight into this CTA's shared memory
-    for (int s = 0; s < kNS; ++s)
-      if (last_g[s] >= 0) {
+    for (int u = 0; u < kPairs; ++u)
+      if (last_n[u] >= 0) {
         const uint64_t t_0 = cycles();
-        while (!mbar_try_wait(bar(B_FULL + s), (last_g[s] / kNS) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
+        while (!mbar_try_wait(bar(B_FULL + u), (last_n[u] / kPairs) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
+      }
+    for (int u = 0; u < kRopes; ++u)
+      if (last_r[u] >= 0) {
+        const uint64_t t_0 = cycles();
+        while (!mbar_try_wait(bar(B_RFULL + u), (last_r[u] / kRopes) & 1) && cycles() - t_0 < kDrainLimitCycles) {}
       }
     if (q_last >= 0) {
       const uint64_t t_0 = cycles();
@@ -184,23 +226,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!failed && it.next(pc)) {
         if (!wait(bar(B_QFULL), k & 1, guard)) break;
         for (int t = pc.t0; t < pc.t1; ++t, ++g) {
-          const int s = g % kNS, sbuf = g & 1;
-          if (!wait(bar(B_FULL + s), (g / kNS) & 1, guard) ||
-              !wait(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard)) {
+          const int sbuf = g & 1;
+          // S^T accumulates chunk by chunk in any order: the RoPE chunk and
+          // the latent pairs are each multiplied as soon as they have landed,
+          // so that only the last pair's MMAs follow the last copy (that
+          // pair's unit is freed by the P . V two tiles back, the others'
+          // by the one three tiles back)
+          if (!wait(bar(B_SEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard) ||
+              !wait(bar(B_RFULL + g % kRopes), (g / kRopes) & 1, guard)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          const uint32_t slot = sb + OFF_RING + s * kTileBytes;
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            const uint64_t d_k = sdesc_sw128(slot + c * kChunkBytes, 16, 1024);
+          auto issue_chunk = [&](int c, bool first) {
+            const uint64_t d_k = sdesc_sw128(chunk_addr(sb, g, c), 16, 1024);
             const uint64_t d_q = sdesc_sw128(sb + OFF_Q + c * kQChunk, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_ss(tmem + 16u * sbuf, d_k + 2u * kk, d_q + 2u * kk, idesc_qk, (c | kk) ? 1u : 0u);
+              umma_ss(tmem + 16u * sbuf, d_k + 2u * kk, d_q + 2u * kk, idesc_qk, (first && kk == 0) ? 0u : 1u);
+          };
+          issue_chunk(8, true);
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            const int n = 4 * g + j;
+            if (!wait(bar(B_FULL + n % kPairs), (n / kPairs) & 1, guard)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            issue_chunk(2 * j, false);
+            issue_chunk(2 * j + 1, false);
           }
+          if (failed) break;
           umma_commit(bar(B_SFULL + sbuf));
+          umma_commit(bar(B_REMPTY + g % kRopes));  // only S^T reads the RoPE chunk
         }
         if (failed) break;
         umma_commit(bar(B_QEMPTY));  // Q of the piece is free once its last S^T is done
@@ -218,18 +277,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const bool first = t == pc.t0;
-          const uint32_t slot = sb + OFF_RING + (g % kNS) * kTileBytes;
           const uint64_t d_p = sdesc_sw128(sb + OFF_P + (g & 1) * kPBytes, 16, 1024);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            // V^T block j: dims [128j, 128j+128) = chunks 2j, 2j+1; +128 per 16 tokens
-            const uint64_t d_v = sdesc_sw128(slot + 2 * j * kChunkBytes, kChunkBytes, 1024);
+            // V^T block j: dims [128j, 128j+128) = chunks 2j, 2j+1 (one ring
+            // unit, chunks 8 KB apart); +128 per 16 tokens
+            const uint64_t d_v = sdesc_sw128(pair_addr(sb, 4 * g + j), kChunkBytes, 1024);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_ss(tmem + kColO + 16u * j, d_v + 128u * kk, d_p + 2u * kk, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            // the unit is free once its block is done: pair 0's unit, freed
+            // first, is the one that the last pair of tile g + 2 waits for
+            umma_commit(bar(B_EMPTY + (4 * g + j) % kPairs));
           }
           umma_commit(bar(B_PEMPTY + (g & 1)));
-          umma_commit(bar(B_EMPTY + g % kNS));
         }
         ++k;
       }
@@ -336,10 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // masked tokens: zero their V rows (they may hold NaN; 0 * NaN would leak)
         if (vm != ~0ull) {
-          const uint32_t slot = sb + OFF_RING + (g % kNS) * kTileBytes;
           for (int e = threadIdx.x - 64; e < 64 * 8 * 8; e += 128) {
             const int row = e >> 6, c = (e >> 3) & 7, u = e & 7;  // token, latent chunk, 16-B unit
-            if (!((vm >> row) & 1ull)) st_shared_v4(slot + c * kChunkBytes + row * 128 + u * 16, 0u, 0u, 0u, 0u);
+            if (!((vm >> row) & 1ull)) st_shared_v4(chunk_addr(sb, g, c) + row * 128 + u * 16, 0u, 0u, 0u, 0u);
           }
         }
         // P^T[g&1] is free once P . V of tile g-2 is done

@@ -333,12 +333,13 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   CUtensorMap tm_qr, tm_kv, tm_kvr, tm_sc;
   const bool few_heads = h_q == kFewHeads;
   if (few_heads) {
-    // few heads: Q of one query position and a whole 64-token tile, each one
-    // box of all 9 chunks of 64 dims
+    // few heads: Q of one query position as one box of all 9 chunks of 64
+    // dims; a 64-token tile as four boxes of two latent chunks and one of the
+    // RoPE chunk
     if (!make_map_chunks(&tm_qr, q, dt, (uint64_t)qrows, kFewHeads, 9) ||
-        !make_map_chunks(&tm_kv, kvcache, dt, kvrows, 64, 9))
+        !make_map_chunks(&tm_kv, kvcache, dt, kvrows, 64, 2) || !make_map_chunks(&tm_kvr, kvcache, dt, kvrows, 64, 1))
       return MLA_ERR_CUDA;
-    tm_kvr = tm_sc = tm_kv;
+    tm_sc = tm_kv;
   } else if (!v41 && !make_map(&tm_qr, q, dt, 2, (uint64_t)qrows, kDK, kDK * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return MLA_ERR_CUDA;
   }
@@ -418,9 +419,9 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
     cfg.dynamicSmemBytes = few::kSmemBytes;
     cfg.stream = st;
     if (fp16)
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<true>, tm_qr, tm_kv, p));
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<true>, tm_qr, tm_kv, tm_kvr, p));
     else
-      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<false>, tm_qr, tm_kv, p));
+      MLA_CUDA(cudaLaunchKernelEx(&cfg, few::mla_decode_fewheads_kernel<false>, tm_qr, tm_kv, tm_kvr, p));
   } else if (stages & STAGE_SPLIT) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * parts, 1, 1);
