@@ -340,33 +340,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < kNH; ++h) x[h] = __uint_as_float(r[h]);
           }
         }
-        // tile max of every head: over the 16 token lanes, then over the 4 warps
-        float mx[kNH];
+        // The reference max m of a head moves only when a score exceeds it
+        // by more than 2^8 (so P <= 256). Each thread checks its own token's
+        // scores; only when one of the 128 finds one above m + 8 (always on a
+        // piece's first tile, where m is -inf) are the tile maxima exchanged,
+        // and the result is what the exchange on every tile would give.
+        bool over = false;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          float v = x[h];
-#pragma unroll
-          for (int o = 8; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          mx[h] = v;
-        }
-        if (lane < kNH) {
-          float mine = mx[0];
-#pragma unroll
-          for (int h = 1; h < kNH; ++h) mine = lane == h ? mx[h] : mine;
-          red[q4 * kNH + lane] = mine;
-        }
-        if (named_sync_or(kSoftBar, 128, !okw)) { failed = true; break; }
+        for (int h = 0; h < kNH; ++h) over |= x[h] * sl2 > m[h] + 8.0f;
         bool resc_any = false;
         float alpha[kNH], mu[kNH];
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float mt = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h])) * sl2;
-          const float m_new = fmaxf(m[h], mt);
-          const bool resc = m_new > m[h] + 8.0f;       // lazy rescale: P stays <= 2^8
-          mu[h] = resc ? m_new : m[h];
-          alpha[h] = resc ? exp2_approx(m[h] - m_new) : 1.0f;
-          resc_any |= resc;
-          m[h] = mu[h];
+        for (int h = 0; h < kNH; ++h) { alpha[h] = 1.0f; mu[h] = m[h]; }
+        if (named_sync_or(kSoftBar, 128, over || !okw)) {
+          // tile max of every head: over the 16 token lanes, then over the 4 warps
+          float mx[kNH];
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) {
+            float v = x[h];
+#pragma unroll
+            for (int o = 8; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            mx[h] = v;
+          }
+          if (lane < kNH) {
+            float mine = mx[0];
+#pragma unroll
+            for (int h = 1; h < kNH; ++h) mine = lane == h ? mx[h] : mine;
+            red[q4 * kNH + lane] = mine;
+          }
+          if (named_sync_or(kSoftBar, 128, !okw)) { failed = true; break; }
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) {
+            const float mt = fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h])) * sl2;
+            const float m_new = fmaxf(m[h], mt);
+            const bool resc = m_new > m[h] + 8.0f;       // lazy rescale: P stays <= 2^8
+            mu[h] = resc ? m_new : m[h];
+            alpha[h] = resc ? exp2_approx(m[h] - m_new) : 1.0f;
+            resc_any |= resc;
+            m[h] = mu[h];
+          }
         }
         // P^T of this tile; this thread's share of each head's sum
         uint32_t pk[kNH / 2];
