@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool over = false;
 #pragma unroll
         for (int h = 0; h < kNH; ++h) over |= x[h] * sl2 > m[h] + 8.0f;
+        // P^T[g&1] is free once P . V of tile g-2 is done; a wait that gave
+        // up is agreed on at the vote below
+        if (okw) okw = warp_all(wait(bar(B_PEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard));
         bool resc_any = false;
         float alpha[kNH], mu[kNH];
 #pragma unroll
@@ -390,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           l[h + 1] = l[h + 1] * alpha[h + 1] + p1;
           pk[h / 2] = kFp16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
-        // a rescale of O^T needs every earlier P . V done (they complete in order)
+        // a rescale of O^T needs every earlier P . V done (they complete in
+        // order); resc_any is the same in every thread, and so is this barrier
         if (resc_any && t != pc.t0) {
           if (!warp_all(wait(bar(B_PEMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1, guard))) failed = true;
           if (warp_all(!failed)) {
@@ -406,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
           }
+          if (named_sync_or(kSoftBar, 128, failed)) { failed = true; break; }
         }
         // masked tokens: zero their V rows (they may hold NaN; 0 * NaN would leak)
         if (vm != ~0ull) {
@@ -414,9 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!((vm >> row) & 1ull)) st_shared_v4(chunk_addr(sb, g, c) + row * 128 + u * 16, 0u, 0u, 0u, 0u);
           }
         }
-        // P^T[g&1] is free once P . V of tile g-2 is done
-        if (!failed && !warp_all(wait(bar(B_PEMPTY + sbuf), ((g >> 1) & 1) ^ 1, guard))) failed = true;
-        if (named_sync_or(kSoftBar, 128, failed)) { failed = true; break; }
         if (has_tok) {
           // [head][token] with 16-B units of each 128-B head row swizzled by (head & 7)
           uint8_t* prow = smem + OFF_P + sbuf * kPBytes;
