@@ -10,11 +10,14 @@
 // and the epilogue writes O^T / l transposed back into [head][dim] order.
 // The work is bound by the cache bytes (about 30 FLOP per byte), so one CTA
 // per SM streams 64-token tiles; no pairing is needed because O^T is only 64
-// TMEM columns. How many bytes each SM keeps in flight sets the rate, so the
-// ring is cut finer than a 72 KB tile: 11 units of two latent chunks (16 KB,
-// the V^T block of 128 dims that one P . V MMA reads) and 3 RoPE chunks (8 KB,
-// read only by S^T and freed as soon as it completes), 2.75 tiles in all,
-// where two whole-tile slots are all that fit beside Q and P.
+// TMEM columns. A tile's turnaround (its slot freed by a P . V, the copy, the
+// S^T MMAs, the softmax, its own P . V) is shared by the tiles in flight, so
+// the ring is cut finer than a 72 KB tile: 11 units of two latent chunks
+// (16 KB, the V^T block of 128 dims that one P . V MMA reads) and 3 RoPE
+// chunks (8 KB, read only by S^T and freed as soon as it completes), 2.75
+// tiles in all, where two whole-tile slots are all that fit beside Q and P.
+// S^T multiplies each unit as soon as it lands, so only the last pair of a
+// tile (whose unit the P . V two tiles back frees) is on the turnaround.
 //
 // Memory map. TMEM (128 columns): S^T buffers [0,16) and [16,32), O^T blocks
 // [64 + 16j, 80 + 16j) for dims [128j, 128j+128). Shared memory: the unit ring
