@@ -39,11 +39,11 @@ WORKLOADS = {
                                               causal=True),
     # 656-byte FP8 cache, paged, per-row outlier channels x8
     "fp8_dense_b16_l32768": dict(kind="fp8", batch=16, s_q=1, lens=("fixed", 32768), causal=False),
-    # few heads (h_q=16, fp16, identity block table): the transposed kernel
-    # (only sizes whose cache exceeds the 129 MB L2: the timed loop does not flush it)
-    "fewheads_fp16_h16_b16_l8192": dict(kind="few", batch=16, s_q=1, lens=("fixed", 8192), causal=False, h_q=16),
-    "fewheads_fp16_h16_b16_l65536": dict(kind="few", batch=16, s_q=1, lens=("fixed", 65536), causal=False, h_q=16),
-    "fewheads_fp16_h16_b32_l65536": dict(kind="few", batch=32, s_q=1, lens=("fixed", 65536), causal=False, h_q=16),
+    # few heads (h_q=16, fp16, identity block table): the transposed kernel,
+    # B in {16, 32} over lengths 512 .. 64K (below, added in a loop); a cache
+    # smaller than twice the 129 MB L2 is one of several block-table sets that
+    # the steps rotate through, so that more than twice the L2 passes between
+    # two uses of one set
     # token-sparse over a 131072-token FP8 cache per request, 5% of the slots -1
     "fp8_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False),
     "fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False),
@@ -65,6 +65,10 @@ WORKLOADS = {
     # headline's 64 query tokens x 128 heads; L2 flushed before every step
     "absorb_bf16_t64_h128": dict(kind="absorb", batch=64, s_q=1, h_q=128, causal=False),
 }
+for _b in (16, 32):
+    for _l in (512, 1024, 2048, 4096, 8192, 16384, 32768, 65536):
+        WORKLOADS[f"fewheads_fp16_h16_b{_b}_l{_l}"] = dict(kind="few", batch=_b, s_q=1, lens=("fixed", _l),
+                                                          causal=False, h_q=16)
 SPARSE_TOKENS = 131072
 DEFAULT_WORKLOAD = "dense_bf16_b64_sq1_l8192"
 L2_BYTES = 129e6       # GB300 L2; a workload whose touched bytes per step are below
@@ -243,12 +247,21 @@ def build_case(w, device):
         return case, None
     seqlens = workload_seqlens(w)
     if w["kind"] == "few":
-        case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=w["h_q"], dtype=torch_dtype("float16"),
-                                     causal=w["causal"], seed=0, device=device, shuffle=False)
+        # requests of block-table set k are k*B .. k*B+B-1 (see few_table_sets)
+        case = synth.make_dense_case(seqlens * few_table_sets(seqlens), s_q=w["s_q"], h_q=w["h_q"],
+                                     dtype=torch_dtype("float16"), causal=w["causal"], seed=0, device=device,
+                                     shuffle=False)
         return case, seqlens
     case = synth.make_dense_case(seqlens, s_q=w["s_q"], h_q=128, causal=w["causal"], seed=0, device=device,
                                  outlier_channels=4 if w["kind"] == "fp8" else 0, d_k=d_k)
     return case, seqlens
+
+
+def few_table_sets(seqlens):
+    """Block-table sets a few-heads workload rotates through: enough that more
+    than twice the L2 is read between two uses of one set."""
+    kv_bytes = sum(seqlens) * 1152
+    return max(1, math.ceil(2 * L2_BYTES / kv_bytes))
 
 
 def torch_dtype(name):
@@ -358,6 +371,10 @@ def run_ours(args, w, rank, world, device):
     else:
         bt = case.block_table.to(device)
         sl = case.cache_seqlens.to(device)
+        if kind == "few":
+            B = len(seqlens)
+            bt_sets = [bt[k * B:(k + 1) * B].contiguous() for k in range(few_table_sets(seqlens))]
+            bt, sl, q = bt_sets[0], sl[:B].contiguous(), q[:B].contiguous()
         if kind == "fp8":
             raw = getattr(mla, qname)(case.kv_rows)
             kv = raw.view(case.num_blocks, 64, 1, row_bytes)
@@ -371,13 +388,16 @@ def run_ours(args, w, rank, world, device):
     stream = torch.cuda.current_stream(device)
     dec_kw = dict(softmax_scale=case.softmax_scale, causal=causal, kv_format=fmt_code)
 
+    if kind != "few":
+        bt_sets = [bt]
+
     def step(k=0):
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
-        mla.mla_decode_with_kvcache(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=idx_sets[k % len(idx_sets)],
-                                    **dec_kw)
+        mla.mla_decode_with_kvcache(q, kv, bt_sets[k % len(bt_sets)], sl, 512, m, n, out=out, lse=lse,
+                                    indices=idx_sets[k % len(idx_sets)], **dec_kw)
 
     # correctness gate before timing: device status must be clean
-    for k in range(len(idx_sets)):
+    for k in range(max(len(idx_sets), len(bt_sets))):
         step(k)
     st, bits = mla.mla_read_status(device=device)
     if st != 0:
@@ -386,18 +406,51 @@ def run_ours(args, w, rank, world, device):
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize(device)
+    n_sets = max(len(idx_sets), len(bt_sets))
+    graph = None
+    if args.graph:
+        # one graph of n_sets consecutive steps (every rotated set once), with
+        # the workspace fixed outside it; replayed steps/n_sets times
+        ws = torch.zeros(mla.load_library().mla_workspace_size(q.shape[0], s_q, h_q, meta.parts), dtype=torch.uint8,
+                         device=device)
+        step_ws = step
+
+        def step(k=0):  # noqa: F811 - the same step with a fixed workspace
+            m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
+            mla.mla_decode_with_kvcache(q, kv, bt_sets[k % len(bt_sets)], sl, 512, m, n, out=out, lse=lse,
+                                        indices=idx_sets[k % len(idx_sets)], workspace=ws, **dec_kw)
+
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for k in range(n_sets):
+                step(k)
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(n_sets):
+                step(k)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        step = step_ws
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
+    n_timed = args.steps if graph is None else n_sets * max(1, args.steps // n_sets)
     with ClockSampler(device.index) as clk:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k in range(args.steps):
-            step(k)
+        if graph is None:
+            for k in range(args.steps):
+                step(k)
+        else:
+            for _ in range(n_timed // n_sets):
+                graph.replay()
         e1.record(stream)
         torch.cuda.synchronize(device)
-    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device)
+    elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) * args.steps / n_timed
     if world > 1:
         torch.distributed.barrier()
     st, bits = mla.mla_read_status(device=device)
@@ -410,10 +463,10 @@ def run_ours(args, w, rank, world, device):
         ev[k][0].record(stream)
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
         ev[k][1].record(stream)
-        ik = idx_sets[k % len(idx_sets)]
-        mla.mla_decode_splitkv(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
+        ik, bk = idx_sets[k % len(idx_sets)], bt_sets[k % len(bt_sets)]
+        mla.mla_decode_splitkv(q, kv, bk, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
         ev[k][2].record(stream)
-        mla.mla_combine_splits(q, kv, bt, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
+        mla.mla_combine_splits(q, kv, bk, sl, 512, m, n, out=out, lse=lse, indices=ik, **dec_kw)
         ev[k][3].record(stream)
     torch.cuda.synchronize(device)
     t_meta = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
@@ -432,6 +485,7 @@ def run_ours(args, w, rank, world, device):
         nbuf = 2
         host_in = [q.cpu().pin_memory()] + [t.cpu().pin_memory() for t in (bt, sl, idx) if t is not None]
         host_idx = [t.cpu().pin_memory() for t in idx_sets] if idx is not None else None
+        host_bt = [t.cpu().pin_memory() for t in bt_sets] if bt is not None and len(bt_sets) > 1 else None
         dev_in = [[torch.empty_like(h, device=device) for h in host_in] for _ in range(nbuf)]
         outs = [torch.empty_like(out) for _ in range(nbuf)]
         lses = [torch.empty_like(lse) for _ in range(nbuf)]
@@ -449,6 +503,8 @@ def run_ours(args, w, rank, world, device):
                 srcs = list(host_in)
                 if host_idx is not None:             # the index set of this step (rotated as above)
                     srcs[-1] = host_idx[k % len(host_idx)]
+                if host_bt is not None:              # the block-table set of this step
+                    srcs[1] = host_bt[k % len(host_bt)]
                 for hsrc, ddst in zip(srcs, dev_in[j]):
                     ddst.copy_(hsrc, non_blocking=True)
                 ev_in[j].record(s_in)
@@ -485,7 +541,7 @@ def run_ours(args, w, rank, world, device):
                "ms_per_step": round(t_e2e * 1e3, 4), "pipelined_buffers": nbuf}
     return dict(elapsed=elapsed, flops=flops, algo_bytes=algo_bytes, kv_bytes=kv_bytes, t_meta=t_meta, t_dec=t_dec,
                 t_comb=t_comb, clocks=clk.summary(), e2e=e2e, parts=meta.parts, case=case, seqlens=seqlens,
-                raw=raw if is_fp8 else None, n_sets=len(idx_sets))
+                raw=raw if is_fp8 else None, n_sets=max(len(idx_sets), len(bt_sets)), graph=graph is not None)
 
 
 def run_absorb(args, w, world, device, hbm_peak, tc_peak, peak_src):
@@ -583,6 +639,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph of the steps (schedule + decode + combine), so that the "
+                         "host's per-call cost drops out of small steps")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -657,10 +716,11 @@ def main():
                                else f"all {w['lens'][1]}" if w["lens"][0] == "fixed"
                                else f"uniform [{w['lens'][1]},{w['lens'][2]}] seed 2"),
                    "parallelism": f"replicas x{world}", "num_sm_parts": r["parts"],
+                   "launch": "CUDA graph replays" if r["graph"] else "calls on the stream",
                    "l2": ("inputs larger than L2 (KV cache %.0f MB per replica)" % (r["kv_bytes"] / 1e6)
                           if r["n_sets"] == 1 else
-                          "inputs larger than L2: %d index sets rotated, %.0f MB of rows each"
-                          % (r["n_sets"], r["kv_bytes"] / 1e6))},
+                          "inputs larger than L2: %d %s sets rotated, %.0f MB of rows each"
+                          % (r["n_sets"], "index" if w["kind"] == "sparse" else "block-table", r["kv_bytes"] / 1e6))},
         "kv_gbs": round(kv_gbs, 1), "algo_gbs": round(world * r["algo_bytes"] / t_step / 1e9, 1),
         "roofline_time_frac": round(t_roof / t_step, 4),
         "kernel_us": {"metadata": round(r["t_meta"] * 1e6, 2), "decode": round(r["t_dec"] * 1e6, 2),
