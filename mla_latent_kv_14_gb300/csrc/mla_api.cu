@@ -448,7 +448,8 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   cudaLaunchConfig_t cc = {};
   // 16 heads: 8 blocks per request share its 64 output units (no row is
   // flagged for an exact recompute there, which every block would repeat)
-  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, c.exact_flags == nullptr && h_q <= 16 ? 8 : 1);
+  const bool z8 = c.exact_flags == nullptr && h_q <= 16;
+  cc.gridDim = dim3(batch * s_q, (h_q + 15) / 16, z8 ? 8 : 1);
   cc.blockDim = dim3(256, 1, 1);
   cc.stream = st;
   cudaLaunchAttribute at[1];
@@ -456,10 +457,14 @@ mla_status decode_impl(int stages, const void* q, int q_dtype, const void* kvcac
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cc.attrs = at;
   cc.numAttrs = 1;
-  if (fp16)
-    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__half>, c));
+  if (fp16 && z8)
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__half, 1>, c));
+  else if (fp16)
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__half, 8>, c));
+  else if (z8)
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__nv_bfloat16, 1>, c));
   else
-    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__nv_bfloat16>, c));
+    MLA_CUDA(cudaLaunchKernelEx(&cc, mla_combine_kernel<__nv_bfloat16, 8>, c));
   return MLA_OK;
 }
 }  // namespace

@@ -486,7 +486,9 @@ __device__ void exact_head(const CombineParams& p, int b, int i, int h) {
 // block = 256: 16 heads per block, each thread 32 of one head's 512 dims.
 // Requests with a single piece were finished by the decode kernel; requests
 // with no visible token get out = 0, lse = -inf here.
-template <typename OutT>
+// kNu: units of 8 dims per thread, 8 / gridDim.z (8 with one block per 16
+// heads, 1 when eight blocks share them).
+template <typename OutT, int kNu>
 __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   pdl_launch_dependents();  // a following schedule kernel may launch; it waits for this grid
   pdl_wait();  // the decode grid has completed and its writes are visible
@@ -510,15 +512,14 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   }
   if (ns == 1) return;
   // Thread t merges, for head 16*blockIdx.y + hl, four dims (4*half ..
-  // 4*half+3) of each of nu units of 8 dims, units u0 .. u0+nu-1. The 32
+  // 4*half+3) of each of kNu units of 8 dims, units u0 .. u0+kNu-1. The 32
   // threads of a warp then read one unit of 16 heads, 512 contiguous bytes of
   // the o_part layout (opart_index). gridDim.z blocks share a request's 64
   // units (more blocks when there are few heads; 1 whenever rows may be
   // flagged for the exact recompute above, which each block would redo).
   const int t = threadIdx.x;
   const int hl = (t >> 1) & 15, half = t & 1, ug = t >> 5;
-  const int nu = 8 / (int)gridDim.z;
-  const int u0 = (8 * (int)blockIdx.z + ug) * nu;
+  const int u0 = (8 * (int)blockIdx.z + ug) * kNu;
   const int h = blockIdx.y * 16 + hl;
   if (h >= p.h_q || ((fmask >> hl) & 1u)) return;  // recomputed above
   const int64_t row = ((int64_t)(b * p.s_q + i) * p.h_q + h);
@@ -527,54 +528,53 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(CombineParams p) {
   const int64_t sstride = 64 * ustride;        // and from one split to the next
   const float* src = p.o_part + opart_index(off, p.h_q, h, 8 * u0) + 4 * half;
   const float* lsp = p.lse_part + (int64_t)off * p.h_q + h;
-  // The first two pieces' partials are loaded together with every piece's
-  // lse, so that a request cut once costs one round trip to memory.
-  float4 x0[8], x1[8];
-  float l0 = -INFINITY, l1 = -INFINITY, mx = -INFINITY;
-  if (ns >= 2) {
+  // The first kPre pieces' partials (16 units in all: two pieces of 8 units,
+  // or sixteen of one) are loaded together with every piece's lse, so that a
+  // request cut into up to kPre pieces costs one round trip to memory.
+  constexpr int kPre = 16 / kNu;
+  float4 x[kPre][kNu];
+  float ls[kPre];
+  float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < nu) {
-        x0[k] = *reinterpret_cast<const float4*>(src + k * ustride);
-        x1[k] = *reinterpret_cast<const float4*>(src + sstride + k * ustride);
-      }
-    l0 = lsp[0];
-    l1 = lsp[p.h_q];
-    mx = fmaxf(l0, l1);
-    for (int s = 2; s < ns; ++s) mx = fmaxf(mx, lsp[(int64_t)s * p.h_q]);
+  for (int s = 0; s < kPre; ++s) {
+    ls[s] = -INFINITY;
+    if (s < ns) {
+#pragma unroll
+      for (int k = 0; k < kNu; ++k) x[s][k] = *reinterpret_cast<const float4*>(src + s * sstride + k * ustride);
+      ls[s] = lsp[(int64_t)s * p.h_q];
+    }
   }
-  float4 acc[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < kPre; ++s) mx = fmaxf(mx, ls[s]);
+  for (int s = kPre; s < ns; ++s) mx = fmaxf(mx, lsp[(int64_t)s * p.h_q]);
+  float4 acc[kNu];
+#pragma unroll
+  for (int k = 0; k < kNu; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   // o += e^{lse_s - m} o_s, in the order of the pieces
-  auto add = [&](const float4(&x)[8], float ls) {
-    if (ls == -INFINITY) return;  // an empty piece (m is finite otherwise)
-    const float w = expf(ls - mx);
+  auto add = [&](const float4(&xs)[kNu], float l_s) {
+    if (l_s == -INFINITY) return;  // an empty piece, or none (m is finite otherwise)
+    const float w = expf(l_s - mx);
     wsum += w;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k >= nu) break;
-      acc[k].x += w * x[k].x;
-      acc[k].y += w * x[k].y;
-      acc[k].z += w * x[k].z;
-      acc[k].w += w * x[k].w;
+    for (int k = 0; k < kNu; ++k) {
+      acc[k].x += w * xs[k].x;
+      acc[k].y += w * xs[k].y;
+      acc[k].z += w * xs[k].z;
+      acc[k].w += w * xs[k].w;
     }
   };
-  if (ns >= 2) {
-    add(x0, l0);
-    add(x1, l1);
-    for (int s = 2; s < ns; ++s) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (k < nu) x0[k] = *reinterpret_cast<const float4*>(src + s * sstride + k * ustride);
-      add(x0, lsp[(int64_t)s * p.h_q]);
-    }
+  for (int s = 0; s < kPre; ++s) add(x[s], ls[s]);
+  for (int s = kPre; s < ns; ++s) {
+    float4 xs[kNu];
+#pragma unroll
+    for (int k = 0; k < kNu; ++k) xs[k] = *reinterpret_cast<const float4*>(src + s * sstride + k * ustride);
+    add(xs, lsp[(int64_t)s * p.h_q]);
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if (k >= nu) break;
+  for (int k = 0; k < kNu; ++k) {
     const int d = 8 * (u0 + k) + 4 * half;
     uint32_t lo, hi;
     if constexpr (std::is_same<OutT, __half>::value) {
