@@ -42,8 +42,8 @@ WORKLOADS = {
     # few heads (h_q=16, fp16, identity block table): the transposed kernel,
     # B in {16, 32} over lengths 512 .. 64K (below, added in a loop); a cache
     # smaller than twice the 129 MB L2 is one of several block-table sets that
-    # the steps rotate through, so that more than twice the L2 passes between
-    # two uses of one set
+    # the steps rotate through: a rotation reads at least twice the L2, and at
+    # least the L2 passes between two uses of one set
     # token-sparse over a 131072-token FP8 cache per request, 5% of the slots -1
     "fp8_sparse_b32_sq1_topk2048": dict(kind="sparse", batch=32, s_q=1, topk=2048, causal=False),
     "fp8_sparse_b32_sq1_topk32768": dict(kind="sparse", batch=32, s_q=1, topk=32768, causal=False),
@@ -258,8 +258,9 @@ def build_case(w, device):
 
 
 def few_table_sets(seqlens):
-    """Block-table sets a few-heads workload rotates through: enough that more
-    than twice the L2 is read between two uses of one set."""
+    """Block-table sets a few-heads workload rotates through: the fewest whose
+    rotation reads at least twice the L2 (so that at least the L2 passes
+    between two uses of one set)."""
     kv_bytes = sum(seqlens) * 1152
     return max(1, math.ceil(2 * L2_BYTES / kv_bytes))
 
@@ -355,8 +356,9 @@ def run_ours(args, w, rank, world, device):
         case.kv_rows = None
         kv = raw.view(-1, 64, 1, row_bytes)
         # the rows one step touches may fit in L2 (topk 2048: about 50 MB per
-        # query position); then several seeded index sets are rotated so that
-        # more than twice the L2 passes between two uses of one set
+        # query position); then several seeded index sets are rotated: a
+        # rotation reads at least twice the L2, and at least the L2 passes
+        # between two uses of one set
         sets = [case.indices.numpy()]
         counts = [work_counts(None, s_q, False, row_bytes=row_bytes, indices=sets[0], d_k=d_k)]
         n_sets = max(1, math.ceil(2 * L2_BYTES / counts[0][2]))

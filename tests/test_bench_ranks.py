@@ -51,3 +51,21 @@ def test_two_gloo_ranks_take_the_slowest_time_and_count_all_work():
 def test_single_process_is_its_own_maximum():
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.whole_job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_few_heads_sweep_rotates_sets_until_twice_the_l2():
+    """The h_q=16 sweep: a cache below twice the L2 is one of the fewest
+    block-table sets whose rotation reads at least twice the L2, so that at
+    least the L2 passes between two uses of one set; a larger cache is read
+    as one set."""
+    for b in (16, 32):
+        for l in (512, 1024, 2048, 4096, 8192, 16384, 32768, 65536):
+            w = bench.WORKLOADS[f"fewheads_fp16_h16_b{b}_l{l}"]
+            assert (w["kind"], w["batch"], w["h_q"], w["lens"]) == ("few", b, 16, ("fixed", l))
+            seqlens = bench.workload_seqlens(w)
+            n = bench.few_table_sets(seqlens)
+            per_set = sum(seqlens) * 1152
+            assert n * per_set >= 2 * bench.L2_BYTES
+            if n > 1:
+                assert (n - 1) * per_set < 2 * bench.L2_BYTES     # no more sets than needed
+                assert (n - 1) * per_set >= bench.L2_BYTES        # a set is gone from L2 when it returns
