@@ -133,11 +133,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   // nothing above reads global memory; wait for the kernels this one depends
-  // on (programmatic dependent launch) before the first read
+  // on (programmatic dependent launch) before the first read. The metadata
+  // header is loaded before the lengths are hashed, so that both reads are in
+  // flight together.
   pdl_wait();
+  int32_t hdr[H_WORDS];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 0; w < H_WORDS; ++w) hdr[w] = p.meta[w];
+  }
   const uint32_t fp = warp == 0 ? lengths_hash_warp(p.seqlens, p.batch, p.topk) : 0u;
   if (threadIdx.x == 0) {
-    *ok_flag = metadata_matches(p, kTile, fp) ? 1u : 0u;
+    *ok_flag = header_matches(hdr, p, kTile, fp) ? 1u : 0u;
     if (!*ok_flag) atomicOr(p.status, STATUS_STALE);
     fence_mbar_init();
     if (*ok_flag && p.stall_cycles) {
@@ -170,13 +177,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto raw_page = [&](int b, int t) {
       return t < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + t) : -1;
     };
+    // the part's first block-table entry, read together with its first piece's
+    // own loads (the part's range is checked, so the entry is in bounds)
+    const int pre_v = it.v + 1, pre_t = it.bt < 0 ? 0 : it.bt;
+    const int pre_pg = it.ev >= pre_v ? raw_page(pre_v % p.batch, pre_t) : -1;
     while (!stop && it.next(pc)) {
       const int b = pc.v % p.batch, i = pc.v / p.batch;
       if (!wait(bar(B_QEMPTY), (qn & 1) ^ 1, guard)) break;
       mbar_arrive_expect_tx(bar(B_QFULL), kQBytes);
       tma_load_3d(sb + OFF_Q, &tm_q, bar(B_QFULL), 0, (b * p.s_q + i) * kNH, 0, pol_q);
       q_last = qn++;
-      int pg_next = raw_page(b, pc.t0);  // block-table entries are loaded one tile ahead
+      // block-table entries are loaded one tile ahead
+      int pg_next = (g == 0 && pc.v == pre_v && pc.t0 == pre_t) ? pre_pg : raw_page(b, pc.t0);
       for (int t = pc.t0; t < pc.t1; ++t, ++g) {
         int page = pg_next;
         page = (page < 0 || page >= p.num_blocks) ? 0 : page;  // a bad page is masked by the softmax warps

@@ -215,17 +215,10 @@ __host__ __device__ inline size_t metadata_smem_bytes(int vreq) {
   return (size_t)(vreq + 1) * sizeof(long long) + (size_t)vreq * 3 * sizeof(int);
 }
 
-// True when the metadata was built for exactly this call; `fp` is the
-// lengths fingerprint of this call (lengths_hash_warp).
-__device__ __forceinline__ bool metadata_matches(const DecodeParams& p, int page_block, uint32_t fp) {
-  const int32_t* h = p.meta;
-  return h[H_MAGIC] == kMetaMagic && h[H_BATCH] == p.batch && h[H_SQ] == p.s_q && h[H_HQ] == p.h_q &&
-         h[H_TOPK] == p.topk && h[H_KVFMT] == p.kv_format && h[H_CAUSAL] == p.causal && h[H_PAGE] == page_block &&
-         h[H_PARTS] == p.parts && h[H_VREQ] == p.batch * p.s_q && (uint32_t)h[H_HASH] == fp;
-}
-
-// The same check on a header already loaded into registers (all comparisons
-// evaluated, so the loads can all be in flight together).
+// True when the metadata was built for exactly this call. `h` is its header,
+// already loaded into registers (all comparisons evaluated, so the loads can
+// all be in flight together); `fp` is the lengths fingerprint of this call
+// (lengths_hash_warp).
 __device__ __forceinline__ bool header_matches(const int32_t (&h)[H_WORDS], const DecodeParams& p, int page_block,
                                                uint32_t fp) {
   return (h[H_MAGIC] == kMetaMagic) & (h[H_BATCH] == p.batch) & (h[H_SQ] == p.s_q) & (h[H_HQ] == p.h_q) &

@@ -75,6 +75,18 @@ def test_fewheads_split_invariance(parts):
     assert_close_attn(out, lse, *ref(case), f"h16 parts={parts}")
 
 
+@pytest.mark.parametrize("parts", [2, 5, 9])
+def test_fewheads_many_short_pieces(parts):
+    """Several pieces per CTA, among them empty requests and pieces of one to
+    three tiles that follow longer ones (the producer runs ahead across piece
+    boundaries, the query slot turns over every piece)."""
+    case = synth.make_dense_case([0, 70, 1, 200, 0, 129, 64, 3, 1100, 2], s_q=2, causal=True, h_q=H,
+                                 dtype=torch.float16, seed=79)
+    out, lse = run(case, parts=parts)
+    assert mla.mla_read_status(device=DEV)[0] == 0
+    assert_close_attn(out, lse, *ref(case), f"h16 short pieces parts={parts}")
+
+
 def test_fewheads_causal_s_q2_and_nan_tails():
     case = synth.make_dense_case([300, 64, 1], s_q=2, causal=True, h_q=H, dtype=torch.float16, seed=76,
                                  spare_blocks=2, tail_fill=float("nan"))
