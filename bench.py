@@ -459,9 +459,15 @@ def run_ours(args, w, rank, world, device):
     if st != 0:
         raise RuntimeError(f"device status {st} (bits {bits}) after timing")
 
-    # per-kernel durations (same stream), for the roofline of the dominant kernel
+    # Per-kernel durations (same stream), for the roofline of the dominant
+    # kernel. Every pass starts behind a spin of about 200 us on the GPU
+    # (torch's sleep kernel), during which the host enqueues the pass's three
+    # calls (70-80 us through the binding), so that the events bracket the
+    # kernels' own execution and never a wait for the host. The inputs are the
+    # timed loop's: the rows larger than L2, or rotated sets of them.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.roofline_steps)]
     for k in range(args.roofline_steps):
+        torch.cuda._sleep(400_000)
         ev[k][0].record(stream)
         m, n = mla.mla_get_metadata(sl, s_q, h_q, num_sm_parts=meta.parts, **meta_args)
         ev[k][1].record(stream)
